@@ -1,0 +1,142 @@
+// Entry points that tie the pool, the segments and the kernels together, plus
+// the small host utilities the kernels' launchers share.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace lora {
+
+std::atomic<uint64_t> g_launches{0};
+
+int sm_count(int device) {
+  static int cache[64] = {0};
+  if (device < 0 || device >= 64) return 148;
+  if (cache[device] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 148;
+    cache[device] = v;
+  }
+  return cache[device];
+}
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* addr, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bd[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bd[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  const CUresult r = fn(map, dt, (cuuint32_t)rank, addr, gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+namespace {
+
+bool any_loaded(const lora_pool* pool) {
+  for (int v : pool->h_rank)
+    if (v > 0) return true;
+  return false;
+}
+
+int check_apply(const lora_pool* pool, const lora_segments* seg, const void* x, const float* y, int64_t ldx,
+                int64_t ldy) {
+  if (!pool || !seg || !x || !y) return LORA_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15)) return LORA_ERR_ARG;
+  if (ldx < pool->d_in || ldy < pool->D || (ldx % 8) || (ldy % 4)) return LORA_ERR_ARG;
+  if (seg->N != pool->N) return LORA_ERR_SHAPE;
+  if (seg->T > pool->max_tokens) return LORA_ERR_SHAPE;
+  return LORA_OK;
+}
+
+int apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y, int64_t ldx, int64_t ldy,
+                int stage, cudaStream_t st) {
+  switch (stage) {
+    case 1:
+      return launch_dec_shrink(pool, seg, static_cast<const uint16_t*>(x), ldx, st);
+    case 2:
+      return launch_dec_expand(pool, seg, y, ldy, st);
+    case 3:
+      return launch_tc_shrink(pool, seg, static_cast<const uint16_t*>(x), ldx, st);
+    case 4:
+      return launch_tc_expand(pool, seg, y, ldy, st);
+    default:
+      return LORA_ERR_ARG;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, const void* x, float* y, int64_t ldx,
+                             int64_t ldy, lora_stream_t stream) {
+  const int chk = check_apply(pool, seg, x, y, ldx, ldy);
+  if (chk != LORA_OK) return chk;
+  if (seg->T == 0 || !any_loaded(pool)) return LORA_OK;  // a layer no adapter edits launches nothing
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  for (int stage = 1; stage <= 4; ++stage) {
+    const int r = apply_stage(pool, seg, x, y, ldx, ldy, stage, st);
+    if (r != LORA_OK) return r;
+  }
+  return LORA_OK;
+}
+
+int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y, int64_t ldx,
+                     int64_t ldy, int stage, lora_stream_t stream) {
+  const int chk = check_apply(pool, seg, x, y, ldx, ldy);
+  if (chk != LORA_OK) return chk;
+  if (stage < 1 || stage > 4) return LORA_ERR_ARG;
+  if (seg->T == 0 || !any_loaded(pool)) return LORA_OK;
+  return apply_stage(pool, seg, x, y, ldx, ldy, stage, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* lora_status_string(int status) {
+  switch (status) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_ARG: return "invalid argument (null or misaligned pointer, bad leading dimension)";
+    case LORA_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case LORA_ERR_SLOT: return "adapter slot id out of range";
+    case LORA_ERR_RANK: return "rank out of range";
+    case LORA_ERR_CUDA: return "CUDA runtime error";
+    case LORA_ERR_META: return "routing metadata inconsistent (negative length or lengths != num_tokens)";
+    case LORA_ERR_TIMEOUT: return "a bounded in-kernel wait gave up";
+    default: return "unknown status";
+  }
+}
+
+uint64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

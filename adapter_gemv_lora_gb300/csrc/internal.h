@@ -1,0 +1,97 @@
+// Host-side descriptors and kernel parameter blocks shared by the library's
+// translation units.  Not part of the public ABI (see include/lora_delta.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <vector>
+
+#include "lora_delta.h"
+
+namespace lora {
+
+// Decode path tiling.
+constexpr int kDecGroup = LORA_DEC_GROUP_ROWS;  // rows of one slot per decode group
+constexpr int kDecKChunk = 2048;                // d_in elements per shrink item
+constexpr int kDecNChunk = 1024;                // output columns per expand item
+constexpr int kDecThreads = 128;
+
+// Tensor path tiling.
+constexpr int kTcTile = LORA_TC_TILE_ROWS;  // MMA M
+constexpr int kTcKBlock = 64;               // d_in elements per TMA stage (128 B of bf16)
+constexpr int kTcNT = 128;                  // expand MMA N per accumulator buffer
+constexpr int kTcNGroup = 1024;             // output columns per expand item
+constexpr int kTcThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+
+inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
+inline int ceil_div(int v, int m) { return (v + m - 1) / m; }
+
+struct TmapLanes {
+  CUtensorMap m[LORA_MAX_LANES];
+};
+
+}  // namespace lora
+
+struct lora_pool {
+  int device = 0;
+  int N = 0, R = 0, R16 = 0, d_in = 0, L = 0, D = 0, max_tokens = 0, C_dec = 0;
+  int d_out[LORA_MAX_LANES] = {0, 0, 0, 0};
+  int off[LORA_MAX_LANES] = {0, 0, 0, 0};
+  char* base = nullptr;
+  size_t bytes = 0;
+  int32_t* rank_tab = nullptr;      // [N][L]
+  float* scale_tab = nullptr;       // [N][L]
+  uint16_t* A[LORA_MAX_LANES] = {};   // per lane [N][R16][d_in]
+  uint16_t* Bt[LORA_MAX_LANES] = {};  // per lane [N][R16][d_out]   (decode expand)
+  uint16_t* Bk[LORA_MAX_LANES] = {};  // per lane [N][d_out][R16]   (tensor expand, K-major)
+  float* u_dec = nullptr;           // [C_dec][max_tokens][L][R16] split-K partial sums
+  float* u_tc = nullptr;            // [max_tokens][L][R16]
+  std::vector<int> h_rank;          // host mirror of rank_tab
+  lora::TmapLanes tm_a;             // A of each lane, 3-D {d_in, R16, N}, box {64,16,1}, SW128
+  lora::TmapLanes tm_bk;            // Bk of each lane, 3-D {R16, d_out, N}, box {16,128,1}, SW32
+};
+
+struct lora_segments {
+  int device = 0;
+  char* ws = nullptr;
+  size_t bytes = 0;
+  int max_seqs = 0, max_tokens = 0, N = 0;
+  int S = 0, T = 0;  // of the last build
+  int cap_dec = 0, cap_tc = 0;
+  int32_t* status = nullptr;
+  int32_t* counts = nullptr;
+  int32_t* seq_start = nullptr;
+  int32_t* seq_pos = nullptr;
+  int32_t* seq_tile = nullptr;
+  int32_t* slot = nullptr;
+  int32_t* perm = nullptr;
+  int32_t* seg_off = nullptr;
+  int4* dec_work = nullptr;
+  int4* tc_work = nullptr;
+};
+
+namespace lora {
+
+extern std::atomic<uint64_t> g_launches;
+int sm_count(int device);
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* addr, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
+
+// Launchers (return a LORA_* status).
+int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens, int S, int T,
+                     cudaStream_t st);
+int launch_repack(lora_pool* pool, int slot, int lane, int rank, float scale, const uint16_t* A,
+                  const uint16_t* B, cudaStream_t st);
+int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                      cudaStream_t st);
+int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy,
+                      cudaStream_t st);
+int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                     cudaStream_t st);
+int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy,
+                     cudaStream_t st);
+
+}  // namespace lora

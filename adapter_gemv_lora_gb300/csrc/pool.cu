@@ -1,0 +1,206 @@
+// The adapter pool of one projection: a fixed number of slots, each holding
+// per lane the bf16 factors of one adapter padded to R16 rows, plus per
+// (slot, lane) rank and fp32 scale tables (xLLM PR #2014, LoRARuntime's
+// per-projection device pool; tokenspeed PR #976, max_loras bounds the slot
+// count; TensorFold PR #47, any rank and scale per module).
+//
+// Layout in the caller's device memory (every region 1024-byte aligned):
+//   rank_tab  int32 [N][L]
+//   scale_tab f32   [N][L]
+//   A_l       bf16  [N][R16][d_in]      per lane; rows >= rank are zero
+//   Bt_l      bf16  [N][R16][d_out_l]   per lane; B transposed, for the decode
+//                                       expand (each rank row is a contiguous
+//                                       run of output columns)
+//   Bk_l      bf16  [N][d_out_l][R16]   per lane; B as given (K-major rows of
+//                                       the rank), for the tensor-core expand
+//   u_dec     f32   [C][max_tokens][L][R16]  decode split-K partial sums
+//   u_tc      f32   [max_tokens][L][R16]     tensor-path rank-space rows
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace lora {
+namespace {
+
+__global__ void repack_kernel(const uint16_t* __restrict__ A, const uint16_t* __restrict__ B, int rank, int R16,
+                              int d_in, int d_out, uint16_t* __restrict__ Ap, uint16_t* __restrict__ Bt,
+                              uint16_t* __restrict__ Bk, int32_t* rank_entry, float* scale_entry, float scale) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t na = (size_t)R16 * d_in, nb = (size_t)R16 * d_out;
+  for (size_t idx = tid; idx < na; idx += stride) {
+    const int i = (int)(idx / d_in), j = (int)(idx % d_in);
+    Ap[idx] = i < rank ? A[(size_t)i * d_in + j] : (uint16_t)0;
+  }
+  for (size_t idx = tid; idx < nb; idx += stride) {
+    const int i = (int)(idx / d_out), o = (int)(idx % d_out);
+    Bt[idx] = i < rank ? B[(size_t)o * rank + i] : (uint16_t)0;
+  }
+  for (size_t idx = tid; idx < nb; idx += stride) {
+    const int o = (int)(idx / R16), i = (int)(idx % R16);
+    Bk[idx] = i < rank ? B[(size_t)o * rank + i] : (uint16_t)0;
+  }
+  if (tid == 0) {
+    *rank_entry = rank;
+    *scale_entry = scale;
+  }
+}
+
+struct PoolLayout {
+  size_t rank_tab, scale_tab, A[LORA_MAX_LANES], Bt[LORA_MAX_LANES], Bk[LORA_MAX_LANES], u_dec, u_tc, total;
+  int R16, C_dec;
+};
+
+size_t align1k(size_t v) { return (v + 1023) & ~(size_t)1023; }
+
+bool pool_layout(int N, int R, int d_in, int L, const int* d_out, int max_tokens, PoolLayout* P) {
+  if (N < 2 || N > LORA_MAX_SLOTS || R < 1 || R > 128 || d_in < 64 || (d_in % 64) || L < 1 || L > LORA_MAX_LANES ||
+      !d_out || max_tokens < 1)
+    return false;
+  const int R16 = round_up(R, 16);
+  if (L * R16 > 256) return false;
+  for (int l = 0; l < L; ++l)
+    if (d_out[l] < 64 || (d_out[l] % 64)) return false;
+  P->R16 = R16;
+  P->C_dec = ceil_div(d_in, kDecKChunk);
+  size_t o = 0;
+  P->rank_tab = o; o = align1k(o + 4 * (size_t)N * L);
+  P->scale_tab = o; o = align1k(o + 4 * (size_t)N * L);
+  for (int l = 0; l < LORA_MAX_LANES; ++l) P->A[l] = P->Bt[l] = P->Bk[l] = 0;
+  for (int l = 0; l < L; ++l) {
+    P->A[l] = o; o = align1k(o + 2 * (size_t)N * R16 * d_in);
+  }
+  for (int l = 0; l < L; ++l) {
+    P->Bt[l] = o; o = align1k(o + 2 * (size_t)N * R16 * d_out[l]);
+  }
+  for (int l = 0; l < L; ++l) {
+    P->Bk[l] = o; o = align1k(o + 2 * (size_t)N * d_out[l] * R16);
+  }
+  P->u_dec = o; o = align1k(o + 4 * (size_t)P->C_dec * max_tokens * L * R16);
+  P->u_tc = o; o = align1k(o + 4 * (size_t)max_tokens * L * R16);
+  P->total = o;
+  return true;
+}
+
+}  // namespace
+
+int launch_repack(lora_pool* pool, int slot, int lane, int rank, float scale, const uint16_t* A, const uint16_t* B,
+                  cudaStream_t st) {
+  const int R16 = pool->R16, d_in = pool->d_in, d_out = pool->d_out[lane];
+  uint16_t* Ap = pool->A[lane] + (size_t)slot * R16 * d_in;
+  uint16_t* Bt = pool->Bt[lane] + (size_t)slot * R16 * d_out;
+  uint16_t* Bk = pool->Bk[lane] + (size_t)slot * d_out * R16;
+  const size_t n = (size_t)R16 * (d_in > d_out ? d_in : d_out);
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  repack_kernel<<<blocks, 256, 0, st>>>(A, B, rank, R16, d_in, d_out, Ap, Bt, Bk,
+                                         pool->rank_tab + slot * pool->L + lane,
+                                         pool->scale_tab + slot * pool->L + lane, scale);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+size_t lora_pool_bytes(int num_slots, int max_rank, int d_in, int num_lanes, const int* lane_d_out,
+                       int max_tokens) {
+  PoolLayout P;
+  return pool_layout(num_slots, max_rank, d_in, num_lanes, lane_d_out, max_tokens, &P) ? P.total : 0;
+}
+
+int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots, int max_rank, int d_in,
+                     int num_lanes, const int* lane_d_out, int max_tokens, lora_stream_t stream) {
+  if (!out || !dev_mem || !lane_d_out || (reinterpret_cast<uintptr_t>(dev_mem) & 255)) return LORA_ERR_ARG;
+  PoolLayout P;
+  if (!pool_layout(num_slots, max_rank, d_in, num_lanes, lane_d_out, max_tokens, &P)) return LORA_ERR_SHAPE;
+  if (bytes < P.total) return LORA_ERR_SHAPE;
+  lora_pool* p = new lora_pool();
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return LORA_ERR_CUDA;
+  }
+  char* b = static_cast<char*>(dev_mem);
+  p->N = num_slots;
+  p->R = max_rank;
+  p->R16 = P.R16;
+  p->d_in = d_in;
+  p->L = num_lanes;
+  p->max_tokens = max_tokens;
+  p->C_dec = P.C_dec;
+  p->base = b;
+  p->bytes = bytes;
+  p->D = 0;
+  for (int l = 0; l < num_lanes; ++l) {
+    p->d_out[l] = lane_d_out[l];
+    p->off[l] = p->D;
+    p->D += lane_d_out[l];
+    p->A[l] = reinterpret_cast<uint16_t*>(b + P.A[l]);
+    p->Bt[l] = reinterpret_cast<uint16_t*>(b + P.Bt[l]);
+    p->Bk[l] = reinterpret_cast<uint16_t*>(b + P.Bk[l]);
+  }
+  p->rank_tab = reinterpret_cast<int32_t*>(b + P.rank_tab);
+  p->scale_tab = reinterpret_cast<float*>(b + P.scale_tab);
+  p->u_dec = reinterpret_cast<float*>(b + P.u_dec);
+  p->u_tc = reinterpret_cast<float*>(b + P.u_tc);
+  p->h_rank.assign((size_t)num_slots * num_lanes, 0);
+  std::memset(&p->tm_a, 0, sizeof(p->tm_a));
+  std::memset(&p->tm_bk, 0, sizeof(p->tm_bk));
+  for (int l = 0; l < num_lanes; ++l) {
+    const uint64_t R16 = (uint64_t)P.R16;
+    {
+      const uint64_t dims[3] = {(uint64_t)d_in, R16, (uint64_t)num_slots};
+      const uint64_t strides[2] = {2ull * d_in, 2ull * d_in * R16};
+      const uint32_t box[3] = {(uint32_t)kTcKBlock, 16u, 1u};
+      if (!encode_tmap(&p->tm_a.m[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->A[l], dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) {
+        delete p;
+        return LORA_ERR_CUDA;
+      }
+    }
+    {
+      const uint64_t dims[3] = {R16, (uint64_t)lane_d_out[l], (uint64_t)num_slots};
+      const uint64_t strides[2] = {2ull * R16, 2ull * R16 * lane_d_out[l]};
+      const uint32_t box[3] = {16u, (uint32_t)kTcNT, 1u};
+      if (!encode_tmap(&p->tm_bk.m[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->Bk[l], dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_32B)) {
+        delete p;
+        return LORA_ERR_CUDA;
+      }
+    }
+  }
+  if (cudaMemsetAsync(dev_mem, 0, P.total, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    delete p;
+    return LORA_ERR_CUDA;
+  }
+  *out = p;
+  return LORA_OK;
+}
+
+int lora_pool_load(lora_pool* pool, int slot, int lane, int rank, float scale, const void* A, const void* B,
+                   lora_stream_t stream) {
+  if (!pool) return LORA_ERR_ARG;
+  if (slot < 1 || slot >= pool->N) return LORA_ERR_SLOT;
+  if (lane < 0 || lane >= pool->L) return LORA_ERR_ARG;
+  if (rank < 0 || rank > pool->R) return LORA_ERR_RANK;
+  if (rank > 0 && (!A || !B)) return LORA_ERR_ARG;
+  if (rank > 0 && (reinterpret_cast<uintptr_t>(A) & 1 || reinterpret_cast<uintptr_t>(B) & 1)) return LORA_ERR_ARG;
+  const int st = launch_repack(pool, slot, lane, rank, rank > 0 ? scale : 0.0f,
+                               static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B),
+                               reinterpret_cast<cudaStream_t>(stream));
+  if (st == LORA_OK) pool->h_rank[(size_t)slot * pool->L + lane] = rank;
+  return st;
+}
+
+int lora_pool_destroy(lora_pool* pool) {
+  delete pool;
+  return LORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,463 @@
+// Segment builder: per-sequence adapter ids and query lengths -> per-token
+// slots, slot-sorted active rows and the decode / tensor work lists.
+//
+// Source of the routing rule: xLLM PR #2014 ("multi-tenant LoRA framework",
+// Wire-up: adapter_ids holds one entry per sequence, index-aligned with
+// q_seq_lens; adapter_ids_per_token is their repeat_interleave; an empty list
+// is a no-op).  Slot 0 = base model (tokenspeed PR #976, RequestSpec::lora_id);
+// base rows enter no segment (TensorFold PR #47: a row of slot 0 is not read
+// or written).  A prompt chunk keeps one slot for all its rows and tiles stay
+// inside a sequence (TensorFold PR #47).
+//
+// One CTA of 1024 threads does all of it; every ordering decision is made by
+// prefix sums or by a warp-ordered pass, never by atomics, so the output is a
+// pure function of the inputs.  Atomics are used only for order-free counts.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace lora {
+namespace {
+
+constexpr int kSegThreads = 1024;
+
+struct SegParams {
+  const int32_t* ids;
+  const int32_t* lens;
+  int S, T, N;
+  int32_t* status;
+  int32_t* counts;
+  int32_t* seq_start;
+  int32_t* seq_pos;
+  int32_t* seq_tile;
+  int32_t* slot;
+  int32_t* perm;
+  int32_t* seg_off;
+  int4* dec_work;
+  int4* tc_work;
+};
+
+// Exclusive prefix sum over the block (all threads call it).  `sums` is a
+// shared array of >= 33 ints.  Returns the prefix and sets `total`.
+__device__ int block_exclusive_scan(int v, int* sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? sums[lane] : 0;
+    int s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sums[lane] = s - w;
+    if (lane == 31) sums[32] = s;
+  }
+  __syncthreads();
+  const int ex = sums[warp] + x - v;
+  total = sums[32];
+  __syncthreads();
+  return ex;
+}
+
+// Largest i in [0, n) with a[i] <= v (a non-decreasing, a[0] <= v).
+__device__ __forceinline__ int last_le(const int32_t* a, int n, int v) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= v) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) {
+  extern __shared__ int smem_dyn[];
+  __shared__ int sums[33];
+  __shared__ int bad_len, bad_id;
+  __shared__ unsigned long long total_len;
+
+  const int N = p.N, S = p.S, T = p.T;
+  int* cnt_tok = smem_dyn;            // [2N]  rows per (class, slot)
+  int* tok_off = cnt_tok + 2 * N;     // [2N]  first perm position of (class, slot)
+  int* run_tok = tok_off + 2 * N;     // [2N]  running position while ranking sequences
+  int* cnt_tile = run_tok + 2 * N;    // [N]   class-1 tiles per slot
+  int* tc_base = cnt_tile + N;        // [N+1] first tile index per slot
+  int* run_tile = tc_base + N + 1;    // [N]
+  int* dec_base = run_tile + N;       // [N+1] first decode group per slot
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // ---- validation
+  if (tid == 0) {
+    bad_len = 0;
+    bad_id = 0;
+    total_len = 0;
+  }
+  for (int i = tid; i < 2 * N; i += kSegThreads) cnt_tok[i] = 0;
+  for (int i = tid; i < N; i += kSegThreads) cnt_tile[i] = 0;
+  __syncthreads();
+  unsigned long long my_sum = 0;
+  for (int s = tid; s < S; s += kSegThreads) {
+    const int len = p.lens[s], id = p.ids[s];
+    if (len < 0) bad_len = 1;
+    if (id < 0 || id >= N) bad_id = 1;
+    my_sum += (unsigned long long)(long long)len;
+  }
+  if (my_sum) atomicAdd(&total_len, my_sum);
+  __syncthreads();
+  if (bad_len || (long long)total_len != (long long)T || bad_id) {
+    if (tid < 4) p.counts[tid] = 0;
+    if (tid == 0) *p.status = (bad_len || (long long)total_len != (long long)T) ? LORA_ERR_META : LORA_ERR_SLOT;
+    return;
+  }
+
+  // ---- seq_start = exclusive prefix of the lengths
+  int carry = 0;
+  for (int b = 0; b < S; b += kSegThreads) {
+    const int s = b + tid;
+    const int v = s < S ? p.lens[s] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, sums, tot);
+    if (s < S) p.seq_start[s] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) p.seq_start[S] = T;
+
+  // ---- histogram of rows per (class, slot) and class-1 tiles per slot
+  for (int s = tid; s < S; s += kSegThreads) {
+    const int len = p.lens[s], id = p.ids[s];
+    if (id != 0 && len > 0) {
+      const int cls = len >= LORA_TC_MIN_QLEN ? 1 : 0;
+      atomicAdd(&cnt_tok[cls * N + id], len);
+      if (cls) atomicAdd(&cnt_tile[id], (len + kTcTile - 1) / kTcTile);
+    }
+  }
+  __syncthreads();
+
+  // ---- offsets: rows (class-major), decode groups per slot, tiles per slot
+  int n_active, n_dec_work, n_tc;
+  carry = 0;
+  for (int b = 0; b < 2 * N; b += kSegThreads) {
+    const int key = b + tid;
+    const int v = key < 2 * N ? cnt_tok[key] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, sums, tot);
+    if (key < 2 * N) tok_off[key] = carry + ex;
+    carry += tot;
+  }
+  n_active = carry;
+  carry = 0;
+  for (int b = 0; b < N; b += kSegThreads) {
+    const int k = b + tid;
+    const int v = k < N ? (cnt_tok[k] + kDecGroup - 1) / kDecGroup : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, sums, tot);
+    if (k < N) dec_base[k] = carry + ex;
+    carry += tot;
+  }
+  n_dec_work = carry;
+  carry = 0;
+  for (int b = 0; b < N; b += kSegThreads) {
+    const int k = b + tid;
+    const int v = k < N ? cnt_tile[k] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, sums, tot);
+    if (k < N) tc_base[k] = carry + ex;
+    carry += tot;
+  }
+  n_tc = carry;
+  if (tid == 0) {
+    dec_base[N] = n_dec_work;
+    tc_base[N] = n_tc;
+  }
+  for (int key = tid; key < 2 * N; key += kSegThreads) run_tok[key] = tok_off[key];
+  for (int k = tid; k < N; k += kSegThreads) run_tile[k] = tc_base[k];
+  for (int i = tid; i < 2 * (N + 1); i += kSegThreads) {
+    const int c = i / (N + 1), k = i % (N + 1);
+    p.seg_off[i] = (k < N) ? tok_off[c * N + k] : (c == 0 ? tok_off[N] : n_active);
+  }
+  __syncthreads();
+
+  // ---- stable rank of each active sequence inside its (class, slot) bin.
+  // Sequences are visited in index order: chunk by chunk, warp by warp; inside
+  // a warp the lanes with the same key take exclusive prefixes of their lengths.
+  for (int b = 0; b < S; b += kSegThreads) {
+    const int s = b + tid;
+    int key = -1, len = 0, nt = 0, id = 0;
+    if (s < S) {
+      len = p.lens[s];
+      id = p.ids[s];
+      if (id != 0 && len > 0) {
+        const int cls = len >= LORA_TC_MIN_QLEN ? 1 : 0;
+        key = cls * N + id;
+        nt = cls ? (len + kTcTile - 1) / kTcTile : 0;
+      }
+    }
+    int pl = 0, pt = 0;
+    bool last = true;
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j) {
+      const int kj = __shfl_sync(0xffffffffu, key, j);
+      const int lj = __shfl_sync(0xffffffffu, len, j);
+      const int tj = __shfl_sync(0xffffffffu, nt, j);
+      if (kj == key) {
+        if (j < lane) {
+          pl += lj;
+          pt += tj;
+        } else if (j > lane) {
+          last = false;
+        }
+      }
+    }
+    const int nwarps = min(32, (S - b + 31) / 32);
+    for (int w = 0; w < nwarps; ++w) {
+      __syncthreads();
+      if (warp == w) {
+        int base_tok = 0, base_tile = 0;
+        if (key >= 0) {
+          base_tok = run_tok[key];
+          if (nt) base_tile = run_tile[id];
+        }
+        __syncwarp();
+        if (key >= 0) {
+          if (last) {
+            run_tok[key] = base_tok + pl + len;
+            if (nt) run_tile[id] = base_tile + pt + nt;
+          }
+          p.seq_pos[s] = base_tok + pl;
+          p.seq_tile[s] = base_tile + pt;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- per-token slot and perm
+  for (int t = tid; t < T; t += kSegThreads) {
+    const int s = last_le(p.seq_start, S + 1, t);
+    const int id = p.ids[s];
+    p.slot[t] = id;
+    if (id != 0) p.perm[p.seq_pos[s] + (t - p.seq_start[s])] = t;
+  }
+
+  // ---- decode groups: slot k's class-0 run cut into runs of <= kDecGroup
+  for (int w = tid; w < n_dec_work; w += kSegThreads) {
+    int lo = 0, hi = N - 1;  // last k with dec_base[k] <= w
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (dec_base[mid] <= w) lo = mid; else hi = mid - 1;
+    }
+    const int k = lo;
+    const int gi = w - dec_base[k];
+    const int pb = tok_off[k] + gi * kDecGroup;
+    const int pe = min(pb + kDecGroup, tok_off[k] + cnt_tok[k]);
+    p.dec_work[w] = make_int4(k, pb, pe, 0);
+  }
+
+  // ---- tensor tiles: each class-1 sequence cut into tiles of <= kTcTile rows
+  for (int s = tid; s < S; s += kSegThreads) {
+    const int len = p.lens[s], id = p.ids[s];
+    if (id != 0 && len >= LORA_TC_MIN_QLEN) {
+      const int st = p.seq_start[s], base = p.seq_tile[s];
+      for (int i = 0, rb = st; rb < st + len; ++i, rb += kTcTile)
+        p.tc_work[base + i] = make_int4(id, rb, min(rb + kTcTile, st + len), s);
+    }
+  }
+
+  if (tid == 0) {
+    p.counts[0] = n_active;
+    p.counts[1] = tok_off[N];
+    p.counts[2] = n_dec_work;
+    p.counts[3] = n_tc;
+    *p.status = LORA_OK;
+  }
+}
+
+size_t seg_smem_bytes(int N) { return sizeof(int) * (size_t)(9 * N + 2); }
+
+}  // namespace
+
+int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens, int S, int T,
+                     cudaStream_t st) {
+  SegParams p;
+  p.ids = ids;
+  p.lens = lens;
+  p.S = S;
+  p.T = T;
+  p.N = seg->N;
+  p.status = seg->status;
+  p.counts = seg->counts;
+  p.seq_start = seg->seq_start;
+  p.seq_pos = seg->seq_pos;
+  p.seq_tile = seg->seq_tile;
+  p.slot = seg->slot;
+  p.perm = seg->perm;
+  p.seg_off = seg->seg_off;
+  p.dec_work = seg->dec_work;
+  p.tc_work = seg->tc_work;
+  const size_t sm = seg_smem_bytes(seg->N);
+  if (sm > 48 * 1024) {
+    if (cudaFuncSetAttribute(seg_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+        cudaSuccess)
+      return LORA_ERR_CUDA;
+  }
+  seg_build_kernel<<<1, kSegThreads, sm, st>>>(p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+namespace {
+
+struct SegLayout {
+  size_t status, counts, seq_start, seq_pos, seq_tile, slot, perm, seg_off, dec_work, tc_work, total;
+  int cap_dec, cap_tc;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool seg_layout(int max_seqs, int max_tokens, int N, SegLayout* L) {
+  if (max_seqs < 1 || max_tokens < 1 || N < 2 || N > LORA_MAX_SLOTS) return false;
+  L->cap_dec = ceil_div(max_tokens, kDecGroup) + N;
+  L->cap_tc = ceil_div(max_tokens, kTcTile) + max_seqs;
+  size_t o = 0;
+  L->status = o; o += 64;
+  L->counts = o; o = align256(o + 64);
+  L->seq_start = o; o = align256(o + 4 * (size_t)(max_seqs + 1));
+  L->seq_pos = o; o = align256(o + 4 * (size_t)max_seqs);
+  L->seq_tile = o; o = align256(o + 4 * (size_t)max_seqs);
+  L->slot = o; o = align256(o + 4 * (size_t)max_tokens);
+  L->perm = o; o = align256(o + 4 * (size_t)max_tokens);
+  L->seg_off = o; o = align256(o + 4 * (size_t)(2 * (N + 1)));
+  L->dec_work = o; o = align256(o + 16 * (size_t)L->cap_dec);
+  L->tc_work = o; o = align256(o + 16 * (size_t)L->cap_tc);
+  L->total = o;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lora_segments_bytes(int max_seqs, int max_tokens, int num_slots) {
+  SegLayout L;
+  return seg_layout(max_seqs, max_tokens, num_slots, &L) ? L.total : 0;
+}
+
+int lora_segments_create(lora_segments** out, void* dev_ws, size_t ws_bytes, int max_seqs, int max_tokens,
+                         int num_slots) {
+  if (!out || !dev_ws || (reinterpret_cast<uintptr_t>(dev_ws) & 255)) return LORA_ERR_ARG;
+  SegLayout L;
+  if (!seg_layout(max_seqs, max_tokens, num_slots, &L)) return LORA_ERR_SHAPE;
+  if (ws_bytes < L.total) return LORA_ERR_SHAPE;
+  lora_segments* s = new lora_segments();
+  if (cudaGetDevice(&s->device) != cudaSuccess) {
+    delete s;
+    return LORA_ERR_CUDA;
+  }
+  char* b = static_cast<char*>(dev_ws);
+  s->ws = b;
+  s->bytes = ws_bytes;
+  s->max_seqs = max_seqs;
+  s->max_tokens = max_tokens;
+  s->N = num_slots;
+  s->cap_dec = L.cap_dec;
+  s->cap_tc = L.cap_tc;
+  s->status = reinterpret_cast<int32_t*>(b + L.status);
+  s->counts = reinterpret_cast<int32_t*>(b + L.counts);
+  s->seq_start = reinterpret_cast<int32_t*>(b + L.seq_start);
+  s->seq_pos = reinterpret_cast<int32_t*>(b + L.seq_pos);
+  s->seq_tile = reinterpret_cast<int32_t*>(b + L.seq_tile);
+  s->slot = reinterpret_cast<int32_t*>(b + L.slot);
+  s->perm = reinterpret_cast<int32_t*>(b + L.perm);
+  s->seg_off = reinterpret_cast<int32_t*>(b + L.seg_off);
+  s->dec_work = reinterpret_cast<int4*>(b + L.dec_work);
+  s->tc_work = reinterpret_cast<int4*>(b + L.tc_work);
+  *out = s;
+  return LORA_OK;
+}
+
+int lora_build_segments(lora_segments* seg, const int32_t* adapter_ids, const int32_t* q_seq_lens, int num_seqs,
+                        int num_tokens, lora_stream_t stream) {
+  if (!seg) return LORA_ERR_ARG;
+  if (num_seqs < 0 || num_tokens < 0) return LORA_ERR_SHAPE;
+  if (num_seqs > seg->max_seqs || num_tokens > seg->max_tokens) return LORA_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (num_seqs == 0) {
+    // Empty step (an empty adapter id list): nothing to route, no kernel.
+    if (num_tokens != 0) return LORA_ERR_SHAPE;
+    seg->S = 0;
+    seg->T = 0;
+    if (cudaMemsetAsync(seg->counts, 0, 16, st) != cudaSuccess) return LORA_ERR_CUDA;
+    return cudaMemsetAsync(seg->status, 0, 4, st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  }
+  if (!adapter_ids || !q_seq_lens) return LORA_ERR_ARG;
+  seg->S = num_seqs;
+  seg->T = num_tokens;
+  return launch_seg_build(seg, adapter_ids, q_seq_lens, num_seqs, num_tokens, st);
+}
+
+int lora_segments_capacity(const lora_segments* seg, int* dec_work_cap, int* tc_work_cap) {
+  if (!seg) return LORA_ERR_ARG;
+  if (dec_work_cap) *dec_work_cap = seg->cap_dec;
+  if (tc_work_cap) *tc_work_cap = seg->cap_tc;
+  return LORA_OK;
+}
+
+int lora_segments_read(const lora_segments* seg, int32_t* host_slot, int32_t* host_perm, int32_t* host_seg_off,
+                       int32_t* host_counts, int32_t* host_dec_work, int32_t* host_tc_work, lora_stream_t stream) {
+  if (!seg) return LORA_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t counts[4];
+  if (cudaMemcpyAsync(counts, seg->counts, 16, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LORA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LORA_ERR_CUDA;
+  const int T = seg->T;
+  auto cp = [&](void* dst, const void* src, size_t n) {
+    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  };
+  bool ok = true;
+  if (host_counts) std::memcpy(host_counts, counts, 16);
+  if (host_slot && T > 0) ok &= cp(host_slot, seg->slot, 4 * (size_t)T);
+  if (host_perm) ok &= cp(host_perm, seg->perm, 4 * (size_t)std::max(0, counts[0]));
+  if (host_seg_off) ok &= cp(host_seg_off, seg->seg_off, 4 * (size_t)(2 * (seg->N + 1)));
+  if (host_dec_work) ok &= cp(host_dec_work, seg->dec_work, 16 * (size_t)std::max(0, counts[2]));
+  if (host_tc_work) ok &= cp(host_tc_work, seg->tc_work, 16 * (size_t)std::max(0, counts[3]));
+  if (!ok) return LORA_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+int lora_get_status(const lora_segments* seg, int32_t* host_status, lora_stream_t stream) {
+  if (!seg || !host_status) return LORA_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_status, seg->status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+int lora_clear_status(lora_segments* seg, lora_stream_t stream) {
+  if (!seg) return LORA_ERR_ARG;
+  return cudaMemsetAsync(seg->status, 0, 4, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
+}
+
+int lora_segments_destroy(lora_segments* seg) {
+  delete seg;
+  return LORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,481 @@
+// Tensor path: rows whose own sequence has q_len >= LORA_TC_MIN_QLEN (prompt
+// chunks).  A chunk uses one slot for all its rows (TensorFold PR #47), so a
+// 128-row tile of one sequence is a dense contraction against one adapter:
+//
+//   shrink  U[128][r] = X_tile[128][d_in] . A[k][l]^T       tcgen05, fp32 in TMEM
+//   expand  y_tile[128][n] += scale * (U . B[k][l]^T)        tcgen05, fp32 in TMEM
+//
+// (the delta scale * B @ (A @ x) of TensorFold PR #47; shrink then expand as in
+// xLLM PR #2014).  U stays fp32 between the kernels; for the expand it is split
+// into two bf16 halves, u_hi = bf16(u) and u_lo = bf16(u - u_hi), and both are
+// multiplied by the (exact) bf16 B and accumulated in fp32, so the rank-space
+// vector keeps about 16 significant bits.
+//
+// Kernel structure (one CTA per work item, 6 warps):
+//   warp 0   lane 0 issues TMA loads into a ring of shared-memory stages
+//   warp 1   lane 0 issues tcgen05.mma and tcgen05.commit
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows)
+// Operands: X and A tiles are K-major with the 128-byte swizzle (TMA boxes of
+// 64 bf16); B tiles are K-major with the 32-byte swizzle (boxes of 16 bf16);
+// the U halves are written by the epilogue threads in the plain K-major core
+// matrix layout (8 rows x 16 bytes per core matrix).
+// Each row's arithmetic is independent of every other row of its tile, and the
+// tile of a row is fixed by its own sequence, so a row's bits do not depend on
+// its batch neighbours.  Every mbarrier wait is bounded; a wait that gives up
+// records LORA_ERR_TIMEOUT in the status word and the CTA unwinds.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace lora {
+namespace {
+
+constexpr int kXBoxRows = 32;                          // TMA box rows of X
+constexpr int kXStageBytes = kTcTile * kTcKBlock * 2;  // 16 KB
+constexpr int kMaxStages = 8;
+
+struct TcShrinkParams {
+  const int32_t* counts;
+  const int4* work;
+  const int32_t* rank_tab;
+  float* u_tc;
+  int32_t* status;
+  int L, R16, num_kb, stages, stage_bytes, tmem_cols;
+};
+
+struct TcExpandParams {
+  const int32_t* counts;
+  const int4* work;
+  const int32_t* rank_tab;
+  const float* scale_tab;
+  const float* u_tc;
+  float* y;
+  int32_t* status;
+  int64_t ldy;
+  int L, R16, total_ng;
+  int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES], ng_base[LORA_MAX_LANES + 1];
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ TmapLanes tm_a,
+                     TcShrinkParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int fail_sh;
+
+  if (*p.status != 0) return;
+  const int tile = blockIdx.x;
+  if (tile >= p.counts[3]) return;
+  const int4 wk = p.work[tile];
+  const int k = wk.x, rb = wk.y, re = wk.z;
+  int r16[LORA_MAX_LANES];
+  bool any = false;
+#pragma unroll
+  for (int l = 0; l < LORA_MAX_LANES; ++l) {
+    const int r = l < p.L ? p.rank_tab[k * p.L + l] : 0;
+    r16[l] = r > 0 ? (r + 15) & ~15 : 0;
+    any |= r > 0;
+  }
+  if (!any) return;
+
+  uint8_t* smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&done_bar, 1);
+    fail_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_sh, (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  const int nbox = (re - rb + kXBoxRows - 1) / kXBoxRows;
+  uint32_t tx_bytes = (uint32_t)nbox * kXBoxRows * kTcKBlock * 2;
+#pragma unroll
+  for (int l = 0; l < LORA_MAX_LANES; ++l) tx_bytes += (uint32_t)r16[l] * kTcKBlock * 2;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int s = kb % p.stages;
+        if (kb >= p.stages) {
+          if (!mbar_wait_or_fail(&empty_bar[s], ((kb / p.stages) - 1) & 1, &fail_sh)) {
+            fail_sh = 1;
+            break;
+          }
+        }
+        uint8_t* xs = smem + (size_t)s * p.stage_bytes;
+        uint8_t* as = xs + kXStageBytes;
+        mbar_expect_tx(&full_bar[s], tx_bytes);
+        for (int b = 0; b < nbox; ++b)
+          tma_load_2d(xs + b * kXBoxRows * kTcKBlock * 2, &tm_x, kb * kTcKBlock, rb + kXBoxRows * b, &full_bar[s]);
+#pragma unroll
+        for (int l = 0; l < LORA_MAX_LANES; ++l)
+          for (int q = 0; q < r16[l] / 16; ++q)
+            tma_load_3d(as + (size_t)(l * p.R16 + 16 * q) * kTcKBlock * 2, &tm_a.m[l], kb * kTcKBlock, 16 * q, k,
+                        &full_bar[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int s = kb % p.stages;
+        if (!mbar_wait_or_fail(&full_bar[s], (kb / p.stages) & 1, &fail_sh)) {
+          fail_sh = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t xa = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const uint32_t aa = xa + kXStageBytes;
+#pragma unroll
+        for (int l = 0; l < LORA_MAX_LANES; ++l) {
+          if (r16[l] == 0) continue;
+          const uint32_t idesc = idesc_bf16(kTcTile, r16[l]);
+#pragma unroll
+          for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
+            const uint64_t ad = smem_desc(xa + 32 * kk, 16, 1024, kSwz128);
+            const uint64_t bd = smem_desc(aa + l * p.R16 * kTcKBlock * 2 + 32 * kk, 16, 1024, kSwz128);
+            mma_bf16(tmem + (uint32_t)(l * p.R16), ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&empty_bar[s]);
+      }
+      if (ok) mma_commit(&done_bar);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int t = rb + row;
+    const bool valid = t < re;
+    const bool ok = mbar_wait_or_fail(&done_bar, 0, &fail_sh);
+    if (!ok) fail_sh = 1;
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int l = 0; l < LORA_MAX_LANES; ++l) {
+        for (int q = 0; q < r16[l] / 16; ++q) {
+          float v[16];
+          tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(l * p.R16 + 16 * q), v);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(p.u_tc + ((size_t)t * p.L + l) * p.R16 + 16 * q);
+            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+            dst[2] = make_float4(v[8], v[9], v[10], v[11]);
+            dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+  }
+  if (threadIdx.x == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_expand_kernel(const __grid_constant__ TmapLanes tm_b, const __grid_constant__ CUtensorMap tm_y,
+                     TcExpandParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bfull[2], bempty[2], afull[2], aempty[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int fail_sh;
+
+  if (*p.status != 0) return;
+  const int item = blockIdx.x;
+  const int tile = item / p.total_ng;
+  if (tile >= p.counts[3]) return;
+  const int q = item - tile * p.total_ng;
+  int l = 0;
+  while (l + 1 < p.L && q >= p.ng_base[l + 1]) ++l;
+  const int ng = q - p.ng_base[l];
+  const int4 wk = p.work[tile];
+  const int k = wk.x, rb = wk.y, re = wk.z;
+  const int r = p.rank_tab[k * p.L + l];
+  if (r <= 0) return;
+  const int r16 = (r + 15) & ~15;
+  const int nk = r16 / 16;
+  const int n_begin = ng * kTcNGroup;
+  const int n_end = min(p.d_out[l], n_begin + kTcNGroup);
+  const int nchunks = (n_end - n_begin + kTcNT - 1) / kTcNT;
+  const float sc = p.scale_tab[k * p.L + l];
+
+  // shared memory: [y staging 4 warps x 2 x 4 KB][B stages 2 x R16*256][U hi 128*R16*2][U lo]
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* ystage = smem;
+  uint8_t* bst = smem + 32768;
+  const size_t bstage_bytes = (size_t)p.R16 * kTcNT * 2;
+  uint8_t* uhi = bst + 2 * bstage_bytes;
+  uint8_t* ulo = uhi + (size_t)kTcTile * p.R16 * 2;
+  const uint32_t u_sbo = (uint32_t)(r16 / 8) * 128;  // bytes between 8-row groups of U
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+      mbar_init(&afull[s], 1);
+      mbar_init(&aempty[s], 4);
+    }
+    fail_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_sh, 2 * kTcNT);
+    tmem_relinquish();
+  }
+  // U rows -> bf16 hi / lo halves in the K-major core-matrix layout.
+  if (warp >= 2) {
+    const int m = (warp & 3) * 32 + lane;
+    const int t = rb + m;
+    const bool valid = t < re;
+    const float* urow = p.u_tc + ((size_t)t * p.L + l) * p.R16;
+    for (int kg = 0; kg < r16 / 8; ++kg) {
+      float u[8];
+      if (valid) {
+        const float4 a = *reinterpret_cast<const float4*>(urow + 8 * kg);
+        const float4 b = *reinterpret_cast<const float4*>(urow + 8 * kg + 4);
+        u[0] = a.x; u[1] = a.y; u[2] = a.z; u[3] = a.w; u[4] = b.x; u[5] = b.y; u[6] = b.z; u[7] = b.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = 0.f;
+      }
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(u[2 * e]);
+        const __nv_bfloat16 h1 = __float2bfloat16_rn(u[2 * e + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(u[2 * e] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(u[2 * e + 1] - __bfloat162float(h1));
+        hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      const size_t o = (size_t)(m >> 3) * u_sbo + (size_t)kg * 128 + (size_t)(m & 7) * 16;
+      *reinterpret_cast<uint4*>(uhi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(ulo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        if (c >= 2) {
+          if (!mbar_wait_or_fail(&bempty[s], ((c >> 1) - 1) & 1, &fail_sh)) {
+            fail_sh = 1;
+            break;
+          }
+        }
+        mbar_expect_tx(&bfull[s], (uint32_t)nk * kTcNT * 32);
+        uint8_t* bs = bst + (size_t)s * bstage_bytes;
+        for (int qq = 0; qq < nk; ++qq)
+          tma_load_3d(bs + (size_t)qq * kTcNT * 32, &tm_b.m[l], 16 * qq, n_begin + c * kTcNT, k, &bfull[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t uh = smem_u32(uhi), ul = smem_u32(ulo);
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        if (!mbar_wait_or_fail(&bfull[s], (c >> 1) & 1, &fail_sh)) {
+          fail_sh = 1;
+          break;
+        }
+        if (c >= 2 && !mbar_wait_or_fail(&aempty[s], ((c >> 1) - 1) & 1, &fail_sh)) {
+          fail_sh = 1;
+          break;
+        }
+        tc_fence_after();
+        const int nt = min(kTcNT, n_end - (n_begin + c * kTcNT));
+        const uint32_t idesc = idesc_bf16(kTcTile, nt);
+        const uint32_t d = tmem + (uint32_t)(s * kTcNT);
+        const uint32_t bsa = smem_u32(bst + (size_t)s * bstage_bytes);
+        for (int qq = 0; qq < nk; ++qq) {
+          const uint64_t ad = smem_desc(uh + 256 * qq, 128, u_sbo, kSwzNone);
+          const uint64_t bd = smem_desc(bsa + qq * kTcNT * 32, 16, 256, kSwz32);
+          mma_bf16(d, ad, bd, idesc, qq > 0 ? 1u : 0u);
+        }
+        for (int qq = 0; qq < nk; ++qq) {
+          const uint64_t ad = smem_desc(ul + 256 * qq, 128, u_sbo, kSwzNone);
+          const uint64_t bd = smem_desc(bsa + qq * kTcNT * 32, 16, 256, kSwz32);
+          mma_bf16(d, ad, bd, idesc, 1u);
+        }
+        mma_commit(&bempty[s]);
+        mma_commit(&afull[s]);
+      }
+    }
+  } else {
+    const int quad = warp & 3;
+    const int m = quad * 32 + lane;
+    const int t = rb + m;
+    const bool row_valid = t < re;
+    const bool warp_full = rb + quad * 32 + 31 < re;
+    uint8_t* mybuf = ystage + (size_t)(warp - 2) * 2 * 4096;
+    int jj = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1;
+      if (!mbar_wait_or_fail(&afull[s], (c >> 1) & 1, &fail_sh)) {
+        fail_sh = 1;
+        break;
+      }
+      tc_fence_after();
+      const int nt = min(kTcNT, n_end - (n_begin + c * kTcNT));
+      const int col0 = p.off[l] + n_begin + c * kTcNT;
+      for (int j = 0; j < nt / 32; ++j, ++jj) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(s * kTcNT + 32 * j), v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] *= sc;
+        if (warp_full) {
+          uint8_t* buf = mybuf + (jj & 1) * 4096;
+          if (jj >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((ch ^ (lane & 7)) * 16)) =
+                make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tm_y, col0 + 32 * j, rb + quad * 32, buf);
+            bulk_commit();
+          }
+        } else if (row_valid) {
+          float4* yp = reinterpret_cast<float4*>(p.y + (size_t)t * p.ldy + col0 + 32 * j);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            float4 a = yp[ch];
+            a.x += v[4 * ch];
+            a.y += v[4 * ch + 1];
+            a.z += v[4 * ch + 2];
+            a.w += v[4 * ch + 3];
+            yp[ch] = a;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[s]);
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kTcNT);
+  }
+  if (threadIdx.x == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
+}
+
+int tc_tile_bound(const lora_segments* seg) { return ceil_div(seg->T, kTcTile) + seg->S; }
+
+}  // namespace
+
+int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                     cudaStream_t st) {
+  const int grid = tc_tile_bound(seg);
+  if (grid <= 0) return LORA_OK;
+  CUtensorMap tm_x;
+  {
+    const uint64_t dims[2] = {(uint64_t)pool->d_in, (uint64_t)seg->T};
+    const uint64_t strides[1] = {2ull * (uint64_t)ldx};
+    const uint32_t box[2] = {(uint32_t)kTcKBlock, (uint32_t)kXBoxRows};
+    if (!encode_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return LORA_ERR_CUDA;
+  }
+  TcShrinkParams p{};
+  p.counts = seg->counts;
+  p.work = seg->tc_work;
+  p.rank_tab = pool->rank_tab;
+  p.u_tc = pool->u_tc;
+  p.status = seg->status;
+  p.L = pool->L;
+  p.R16 = pool->R16;
+  p.num_kb = pool->d_in / kTcKBlock;
+  p.stage_bytes = kXStageBytes + pool->L * pool->R16 * kTcKBlock * 2;
+  int stages = (200 * 1024) / p.stage_bytes;
+  if (stages > 6) stages = 6;
+  if (stages < 2) stages = 2;
+  p.stages = stages;
+  int cols = 32;
+  while (cols < pool->L * pool->R16) cols <<= 1;
+  p.tmem_cols = cols;
+  const int smem = stages * p.stage_bytes + 1024;
+  if (cudaFuncSetAttribute(tc_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  tc_shrink_kernel<<<grid, kTcThreads, smem, st>>>(tm_x, pool->tm_a, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {
+  TcExpandParams p{};
+  p.ng_base[0] = 0;
+  for (int l = 0; l < LORA_MAX_LANES; ++l) {
+    p.d_out[l] = pool->d_out[l];
+    p.off[l] = pool->off[l];
+    p.ng_base[l + 1] = p.ng_base[l] + (l < pool->L ? ceil_div(pool->d_out[l], kTcNGroup) : 0);
+  }
+  p.total_ng = p.ng_base[pool->L];
+  const long long grid = (long long)tc_tile_bound(seg) * p.total_ng;
+  if (grid <= 0) return LORA_OK;
+  CUtensorMap tm_y;
+  {
+    const uint64_t dims[2] = {(uint64_t)pool->D, (uint64_t)seg->T};
+    const uint64_t strides[1] = {4ull * (uint64_t)ldy};
+    const uint32_t box[2] = {32u, 32u};
+    if (!encode_tmap(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LORA_ERR_CUDA;
+  }
+  p.counts = seg->counts;
+  p.work = seg->tc_work;
+  p.rank_tab = pool->rank_tab;
+  p.scale_tab = pool->scale_tab;
+  p.u_tc = pool->u_tc;
+  p.y = y;
+  p.ldy = ldy;
+  p.status = seg->status;
+  p.L = pool->L;
+  p.R16 = pool->R16;
+  const int smem = 32768 + 4 * kTcTile * pool->R16 * 2 + 1024;  // staging + 2 B stages + U hi/lo
+  if (cudaFuncSetAttribute(tc_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  tc_expand_kernel<<<(unsigned)grid, kTcThreads, smem, st>>>(pool->tm_bk, tm_y, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+}  // namespace lora

@@ -1,0 +1,525 @@
+#!/usr/bin/env python3
+"""Benchmark of the mixed-adapter LoRA delta on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch: lora_build_segments
+(routing metadata) followed, for every projection of the workload, by the four
+kernels of lora_apply_shrink_expand (decode shrink, decode expand, tensor
+shrink, tensor expand).  Inputs are resident in HBM before timing starts.
+Between timed steps y is restored and L2 is flushed (a 256 MiB write), both
+outside the CUDA events that time the step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
+on its own GPU (no data exchange; weak scaling); times are max-reduced.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from adapter_gemv_lora_gb300 import workloads as W  # noqa: E402
+
+METRIC = "LoRA-delta tokens/s; HBM GB/s (decode) & TFLOP/s (prefill) as % roofline"
+TC_MIN_QLEN = 64  # documented tensor-path threshold of the library (own sequence length)
+STAGES = ["dec_shrink", "dec_expand", "tc_shrink", "tc_expand"]
+KERNEL_NAMES = {"dec_shrink": "dec_shrink_kernel", "dec_expand": "dec_expand_kernel",
+                "tc_shrink": "tc_shrink_kernel", "tc_expand": "tc_expand_kernel", "seg_build": "seg_build_kernel"}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_units(wl: W.Workload):
+    """Per projection and per kernel: algorithmic bytes and flops of one step.
+
+    Per active row: 2*d_in bytes of x (shrink) and 8*D bytes of y (fp32 read +
+    write, expand).  Per (slot, lane) present on a path: 2*r*d_in bytes of A
+    (shrink) and 2*r*d_out bytes of B (expand), true rank only.  Base rows and
+    rank-0 lanes cost nothing.  flops = sum over active rows and loaded lanes
+    of 2*r*(d_in + d_out)."""
+    slot = np.repeat(wl.adapter_ids, wl.q_seq_lens)
+    qlen = np.repeat(wl.q_seq_lens, wl.q_seq_lens)
+    cls = (qlen >= TC_MIN_QLEN).astype(np.int64)
+    out = []
+    for proj in wl.projections:
+        u = {s: {"bytes": 0, "flops": 0, "rows": 0} for s in STAGES}
+        for c, (sh, ex) in enumerate([("dec_shrink", "dec_expand"), ("tc_shrink", "tc_expand")]):
+            rows = (slot != 0) & (cls == c)
+            ks = slot[rows]
+            for k in np.unique(ks):
+                n = int((ks == k).sum())
+                for l, dout in enumerate(proj.lane_d_out):
+                    r = int(proj.rank[k, l])
+                    if r <= 0:
+                        continue
+                    u[sh]["bytes"] += 2 * r * proj.d_in
+                    u[ex]["bytes"] += 2 * r * dout
+                    u[sh]["flops"] += n * 2 * r * proj.d_in
+                    u[ex]["flops"] += n * 2 * r * dout
+                loaded = [l for l in range(proj.num_lanes) if proj.rank[k, l] > 0]
+                if loaded:
+                    u[sh]["bytes"] += n * 2 * proj.d_in
+                    u[ex]["bytes"] += n * 8 * sum(proj.lane_d_out[l] for l in loaded)
+                    u[sh]["rows"] += n
+                    u[ex]["rows"] += n
+        out.append(u)
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0].split()[0]))
+                mx.append(float(parts[1].split()[0]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches the kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for ln in open(path):
+        if ":" in ln and not ln.startswith("#"):
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "adapter_gemv_lora_gb300", "csrc",
+                       "tensor.cu" if kernel.startswith("tc_") else "decode.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if vals.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ our arm
+
+def setup_device_workload(wl, dev):
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    T = wl.T
+    projs = []
+    for proj in wl.projections:
+        pool = LD.LoraPool(wl.num_slots, proj.max_rank, proj.d_in, proj.lane_d_out, T, device=dev)
+        for k in range(1, wl.num_slots):
+            for l in range(proj.num_lanes):
+                r = int(proj.rank[k, l])
+                if r > 0:
+                    A = torch.from_numpy(proj.A[k][l].view(np.int16)).to(dev)
+                    B = torch.from_numpy(proj.B[k][l].view(np.int16)).to(dev)
+                    pool.load(k, l, A, B, float(proj.scale[k, l]))
+                    torch.cuda.synchronize()
+        x = torch.from_numpy(proj.x.view(np.int16)).to(dev)
+        y0 = torch.from_numpy(proj.y0).to(dev)
+        y = y0.clone()
+        projs.append({"proj": proj, "pool": pool, "x": x, "y0": y0, "y": y})
+    seg = LD.LoraSegments(wl.S, T, wl.num_slots, device=dev)
+    ids = torch.from_numpy(wl.adapter_ids.astype(np.int32)).to(dev)
+    lens = torch.from_numpy(wl.q_seq_lens.astype(np.int32)).to(dev)
+    return projs, seg, ids, lens
+
+
+def time_ours(wl, steps, warmup, dev, sampler_index):
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    projs, seg, ids, lens = setup_device_workload(wl, dev)
+    T = wl.T
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    n_ev = 2 + 4 * len(projs)
+
+    def one_step(evs):
+        evs[0].record(stream)
+        seg.build(ids, lens, num_tokens=T)
+        evs[1].record(stream)
+        i = 2
+        for pr in projs:
+            for stage in range(1, 5):
+                LD.apply_stage(pr["pool"], seg, pr["x"], pr["y"], stage)
+                evs[i].record(stream)
+                i += 1
+
+    def reset():
+        for pr in projs:
+            pr["y"].copy_(pr["y0"])
+        flush.fill_(1)
+
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    warm = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    for _ in range(warmup):
+        reset()
+        one_step(warm)
+    torch.cuda.synchronize()
+    assert seg.status() == 0, LD.lora_status_string(seg.status())
+    sampler = ClockSampler(sampler_index)
+    with sampler:
+        time.sleep(0.3)
+        barrier()
+        torch.cuda.synchronize()
+        n0 = LD.lora_launch_count()
+        for s in range(steps):
+            reset()
+            one_step(evsets[s])
+        n1 = LD.lora_launch_count()
+        torch.cuda.synchronize()
+        barrier()
+    assert seg.status() == 0, LD.lora_status_string(seg.status())
+    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in evsets]
+    seg_ms = [ev[0].elapsed_time(ev[1]) for ev in evsets]
+    stage_ms = []
+    for p in range(len(projs)):
+        per = {}
+        for j, name in enumerate(STAGES):
+            a, b = 1 + 4 * p + j, 2 + 4 * p + j
+            per[name] = statistics.mean(ev[a].elapsed_time(ev[b]) for ev in evsets)
+        stage_ms.append(per)
+    res = {"step_ms": statistics.mean(step_ms), "step_ms_median": statistics.median(step_ms),
+           "seg_ms": statistics.mean(seg_ms), "stage_ms": stage_ms, "launches": n1 - n0,
+           "clocks": sampler.summary()}
+    del flush
+    return res, (projs, seg, ids, lens)
+
+
+def time_e2e(wl, ctx, steps, warmup, dev):
+    """Same step through the public API with pinned host buffers: H2D of x, y and
+    the routing ids, build + apply, D2H of y, all inside the timed region."""
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    projs, seg, ids, lens = ctx
+    T = wl.T
+    host = []
+    for pr in projs:
+        host.append({"x": torch.from_numpy(pr["proj"].x.view(np.int16)).pin_memory(),
+                     "y0": torch.from_numpy(pr["proj"].y0).pin_memory(),
+                     "out": torch.empty(pr["y"].shape, dtype=torch.float32).pin_memory()})
+    ids_h = torch.from_numpy(wl.adapter_ids.astype(np.int32)).pin_memory()
+    lens_h = torch.from_numpy(wl.q_seq_lens.astype(np.int32)).pin_memory()
+    h2d = sum(h["x"].numel() * 2 + h["y0"].numel() * 4 for h in host) + ids_h.numel() * 4 + lens_h.numel() * 4
+    d2h = sum(h["out"].numel() * 4 for h in host)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        ids.copy_(ids_h, non_blocking=True)
+        lens.copy_(lens_h, non_blocking=True)
+        LD.lora_build_segments(seg.handle, ids.data_ptr(), lens.data_ptr(), wl.S, T, stream.cuda_stream)
+        for pr, h in zip(projs, host):
+            pr["x"].copy_(h["x"], non_blocking=True)
+            pr["y"].copy_(h["y0"], non_blocking=True)
+            LD.apply(pr["pool"], seg, pr["x"], pr["y"])
+            h["out"].copy_(pr["y"], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def cpu_oracle_rate(wl, target_s: float, seed: int = 0):
+    """The oracle (as it is) on host cores over a random sample of the step's rows.
+
+    Returns (rows/s, cores, sample description, seconds)."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    rng = np.random.default_rng(seed)
+    t0 = time.perf_counter()
+    meta = oracle.segments(wl.adapter_ids, wl.q_seq_lens, wl.T, wl.num_slots, TC_MIN_QLEN, 128, 8)
+    t_meta = time.perf_counter() - t0
+    slot = meta["slot"]
+    flats = [oracle.flatten_factors(p) for p in wl.projections]
+
+    def run(n):
+        rows = np.sort(rng.choice(wl.T, size=n, replace=False))
+        t = time.perf_counter()
+        for p, fl in zip(wl.projections, flats):
+            oracle.delta(p, slot, rows=rows, _flat=fl)
+        return time.perf_counter() - t
+
+    n = min(64, wl.T)
+    dt = run(n)
+    while dt < 0.2 * target_s and n < wl.T:
+        n = min(wl.T, max(2 * n, int(n * target_s / max(dt, 1e-3) * 0.5)))
+        dt = run(n)
+    # the metadata of the whole step is part of the path; charge it per sampled row
+    dt_total = dt + t_meta * n / wl.T
+    return n / dt_total, cores, f"{n} of {wl.T} rows of one step (uniform random), fp64, {cores} threads", dt_total
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(v: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return v
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    wl = W.make_workload(args.workload, seed=args.seed + rank)
+    res, ctx = time_ours(wl, args.steps, args.warmup, dev, local)
+    step_ms = max_over_ranks(res["step_ms"])
+    units = algorithmic_units(wl)
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    # per-kernel roofline
+    kernels = {}
+    for p, (u, sm) in enumerate(zip(units, res["stage_ms"])):
+        for name in STAGES:
+            ms = sm[name]
+            b, f = u[name]["bytes"], u[name]["flops"]
+            key = name if len(units) == 1 else f"{wl.projections[p].name}.{name}"
+            kernels[key] = {"ms": round(ms, 5), "alg_bytes": int(b), "flops": int(f),
+                            "gbs": round(b / (ms * 1e-3) / 1e9, 1) if ms > 0 and b else 0.0,
+                            "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4) if ms > 0 and b else 0.0,
+                            "tflops": round(f / (ms * 1e-3) / 1e12, 2) if ms > 0 and f else 0.0}
+    dom_key = max(kernels, key=lambda k: kernels[k]["ms"])
+    dom = kernels[dom_key]
+    stage_name = dom_key.split(".")[-1]
+    traffic = traffic_from_profile(KERNEL_NAMES[stage_name], args.workload)
+    total_bytes = sum(u[s]["bytes"] for u in units for s in STAGES)
+    total_flops = sum(u[s]["flops"] for u in units for s in STAGES)
+    apply_ms = sum(sum(sm.values()) for sm in res["stage_ms"])
+    T = wl.T
+    tokens_per_s = T * ws / (step_ms * 1e-3)
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(wl, ctx, max(3, args.steps // 4), 2, dev)
+        e2e_ms = max_over_ranks(e2e_ms)
+        e2e = {"value": round(T * ws / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        rate, cores, sample, secs = cpu_oracle_rate(wl, args.cpu_seconds)
+        cpu = {"value": round(rate, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": round(secs, 2)}
+    active = int(((np.repeat(wl.adapter_ids, wl.q_seq_lens)) != 0).sum())
+    line = {
+        "metric": METRIC,
+        "value": round(tokens_per_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 accumulate / fp32 y",
+        "data": "synthetic (seeded PCG64; random-init adapters)",
+        "config": {"workload": wl.name, "tokens": T, "active_tokens": active, "sequences": wl.S,
+                   "slots": wl.num_slots,
+                   "projections": [{"name": p.name, "d_in": p.d_in, "lanes": p.lane_d_out, "max_rank": p.max_rank}
+                                   for p in wl.projections],
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                   "parallelism": f"replicas x{ws} (no exchange)"},
+        "roofline": {"kernel": KERNEL_NAMES[stage_name] + (f" ({dom_key})" if "." in dom_key else ""),
+                     "bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(dom["gbs"] / hbm_peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "step_roofline": {"alg_bytes": int(total_bytes), "flops": int(total_flops),
+                          "apply_ms": round(apply_ms, 5), "seg_build_ms": round(res["seg_ms"], 5),
+                          "gbs": round(total_bytes / (apply_ms * 1e-3) / 1e9, 1),
+                          "frac_hbm": round(total_bytes / (apply_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "tflops": round(total_flops / (apply_ms * 1e-3) / 1e12, 2),
+                          "frac_bf16": round(total_flops / (apply_ms * 1e-3) / 1e12 / bf16_peak, 5)},
+        "kernels": kernels,
+        "gpu_launches": int(res["launches"]),
+        "clocks": res["clocks"],
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if args.all_workloads and rank == 0:
+        line["per_workload"] = per_workload_summary(args, dev, hbm_peak)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def per_workload_summary(args, dev, hbm_peak):
+    out = {}
+    for name in W.CONFIG_NAMES:
+        if name == args.workload:
+            continue
+        wl = W.make_workload(name, seed=args.seed)
+        res, _ = time_ours(wl, args.steps, args.warmup, dev, 0)
+        units = algorithmic_units(wl)
+        apply_ms = sum(sum(sm.values()) for sm in res["stage_ms"])
+        b = sum(u[s]["bytes"] for u in units for s in STAGES)
+        f = sum(u[s]["flops"] for u in units for s in STAGES)
+        out[name] = {"tokens": wl.T, "ms_per_step": round(res["step_ms"], 5),
+                     "tokens_per_s": round(wl.T / (res["step_ms"] * 1e-3), 1),
+                     "apply_ms": round(apply_ms, 5), "seg_build_ms": round(res["seg_ms"], 5),
+                     "alg_bytes": int(b), "gbs": round(b / (apply_ms * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(b / (apply_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                     "tflops": round(f / (apply_ms * 1e-3) / 1e12, 2),
+                     "stage_ms": [{k: round(v, 5) for k, v in sm.items()} for sm in res["stage_ms"]]}
+    return out
+
+
+# ------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The CPU oracle, as it is, on the host cores; rank 0 only."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    wl = W.make_workload(args.workload, seed=args.seed, draw_xy=True)
+    per_step_s = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(wl, per_step_s * 0.5)
+    rates, secs = [], []
+    for s in range(args.steps):
+        rate, cores, sample, dt = cpu_oracle_rate(wl, per_step_s, seed=s)
+        rates.append(rate)
+        secs.append(dt)
+    value = statistics.mean(rates)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * wl.T / value, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded PCG64; random-init adapters)",
+        "config": {"workload": wl.name, "tokens": wl.T, "sequences": wl.S, "slots": wl.num_slots},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {sample}"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cont_batch", choices=W.CONFIG_NAMES)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--all-workloads", action="store_true", help="add a per_workload summary of the other configs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * lora_delta.h — C ABI of the GB300 (sm_103a) mixed-adapter LoRA delta.
+ *
+ * One step of multi-tenant LoRA serving adds, for every token row t whose
+ * adapter slot k = slot[t] is not 0,
+ *
+ *     y[t][off_l : off_l + d_out_l] += scale[k][l] * B[k][l] @ (A[k][l] @ x[t])
+ *
+ * for every lane l of the projection (one lane for o_proj / down_proj, three
+ * for fused q,k,v, two for fused gate,up).  The formula, the fp32 partial sum
+ * it is added to, the per-row slot with slot 0 = base (a slot-0 row is neither
+ * read nor written), and per-row determinism come from TensorFold PR #47
+ * ("Add native per-request LoRA adapters to the DeepSeek-V4.1 CUDA engine",
+ * the kernels-and-ranks paragraph).  The shrink / expand split and the lane
+ * shapes (B.size(0) = the lane's output width, GQA k/v lanes narrower than q)
+ * come from xLLM PR #2014 ("multi-tenant LoRA framework", the
+ * LoRAQKVParallelLinear / LoRAColumnParallelLinear / LoRARowParallelLinear
+ * items).  The routing input (one adapter id per sequence, index-aligned with
+ * the query lengths; per-token ids by repeat_interleave; an empty id list is a
+ * no-op) comes from xLLM PR #2014, "Wire-up".  The fixed slot pool sized by
+ * the largest number of distinct adapters in a batch comes from tokenspeed
+ * PR #976 (max_loras).
+ *
+ * Conventions shared by every entry point
+ *  - All device memory is allocated and freed by the caller.  The library
+ *    never allocates device memory and keeps only small host descriptors.
+ *  - Every GPU action is enqueued on the caller's stream (a cudaStream_t; 0 is
+ *    the legacy default stream).  Entry points on the hot path never
+ *    synchronise with the host.
+ *  - Matrices are row-major.  Leading dimensions (ldx, ldy) are in elements.
+ *  - bf16 data is passed as raw 16-bit words (bf16 bit patterns).
+ *  - Host-checkable errors are returned before anything is enqueued.
+ *    Errors found on the device (bad routing metadata, a kernel wait that
+ *    gave up) are written to the segments' status word; read it with
+ *    lora_get_status().  No kernel traps or asserts.
+ *  - Entry points are thread-compatible: calls on distinct objects may run
+ *    concurrently; calls on one object must be serialised by the caller.
+ */
+#ifndef LORA_DELTA_H
+#define LORA_DELTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* lora_stream_t; /* identical to cudaStream_t */
+
+/* Status codes. */
+enum {
+  LORA_OK = 0,
+  LORA_ERR_ARG = -1,     /* null pointer, misaligned pointer, bad leading dimension   */
+  LORA_ERR_SHAPE = -2,   /* unsupported or inconsistent sizes                          */
+  LORA_ERR_SLOT = -3,    /* a slot id outside [0, num_slots) (host or device detected) */
+  LORA_ERR_RANK = -4,    /* rank outside [0, max_rank]                                 */
+  LORA_ERR_CUDA = -5,    /* a CUDA runtime call failed                                 */
+  LORA_ERR_META = -6,    /* device-detected: a negative q_seq_len or sum != num_tokens */
+  LORA_ERR_TIMEOUT = -7  /* device-detected: a bounded in-kernel wait gave up          */
+};
+
+/* Layout constants of the work lists (part of the ABI). */
+#define LORA_MAX_LANES 4         /* lanes per projection                               */
+#define LORA_MAX_SLOTS 2048      /* slots per pool, slot 0 included                    */
+#define LORA_DEC_GROUP_ROWS 8    /* rows per decode work group                         */
+#define LORA_TC_TILE_ROWS 128    /* rows per tensor-path tile                          */
+#define LORA_TC_MIN_QLEN 64      /* a row takes the tensor path iff its own sequence's */
+                                 /* q_seq_len >= this; otherwise the decode path       */
+
+typedef struct lora_pool lora_pool;
+typedef struct lora_segments lora_segments;
+
+/* ------------------------------------------------------------------ pool --
+ * The adapter pool of one projection (xLLM PR #2014, LoRARuntime "per-proj
+ * device pool"; the pool has a fixed number of slots, tokenspeed PR #976;
+ * ranks and scales may differ per slot and per module, TensorFold PR #47).
+ *
+ * Slot 0 is the base model and holds nothing.  Slots 1..num_slots-1 hold, per
+ * lane, bf16 factors of a rank r <= max_rank padded with zeros to
+ * R16 = max_rank rounded up to a multiple of 16, a rank and an fp32 scale
+ * (the caller computes scale = lora_alpha / r * strength).  The pool also
+ * holds the per-row fp32 rank-space scratch of up to max_tokens rows used
+ * between the shrink and the expand kernels, so two applies on one pool must
+ * be ordered on one stream.
+ *
+ * Shapes: d_in and every lane_d_out[l] must be positive multiples of 64;
+ * 1 <= num_lanes <= LORA_MAX_LANES; 2 <= num_slots <= LORA_MAX_SLOTS;
+ * 1 <= max_rank <= 128 and num_lanes * R16 <= 256; max_tokens >= 1.
+ */
+
+/* Bytes of device memory a pool of this shape needs (0 if the shape is invalid). */
+size_t lora_pool_bytes(int num_slots, int max_rank, int d_in, int num_lanes,
+                       const int* lane_d_out /* host [num_lanes] */, int max_tokens);
+
+/* Create a pool descriptor over caller memory dev_mem (>= lora_pool_bytes,
+ * 256-byte aligned).  Enqueues a zero fill of dev_mem on `stream`, so every
+ * slot starts unloaded (rank 0).  The descriptor records the current CUDA
+ * device.  Errors: LORA_ERR_ARG, LORA_ERR_SHAPE, LORA_ERR_CUDA. */
+int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots, int max_rank,
+                     int d_in, int num_lanes, const int* lane_d_out /* host */, int max_tokens,
+                     lora_stream_t stream);
+
+/* Load (or replace) lane `lane` of slot `slot` (1..num_slots-1):
+ *   A: device bf16 [rank][d_in] row-major (PEFT lora_A layout),
+ *   B: device bf16 [lane_d_out[lane]][rank] row-major (PEFT lora_B layout).
+ * rank = 0 unloads the lane (A and B may then be NULL).  The copy/repack is
+ * enqueued on `stream`; A and B must stay valid until it has run.  The caller
+ * must not run this concurrently with an apply that reads the slot.
+ * Errors: LORA_ERR_ARG, LORA_ERR_SLOT, LORA_ERR_RANK, LORA_ERR_CUDA. */
+int lora_pool_load(lora_pool* pool, int slot, int lane, int rank, float scale,
+                   const void* A, const void* B, lora_stream_t stream);
+
+/* Free the host descriptor only (device memory stays the caller's). */
+int lora_pool_destroy(lora_pool* pool);
+
+/* -------------------------------------------------------------- segments --
+ * Routing metadata of one step, shared by every layer and projection of that
+ * step.  Built on the device from per-sequence adapter ids and query lengths
+ * (xLLM PR #2014, Wire-up: adapter_ids index-aligned with q_seq_lens,
+ * adapter_ids_per_token by repeat_interleave).  Contents after a build:
+ *   slot[T]       per-token slot
+ *   perm[]        active rows (slot != 0) ordered by (class, slot, row), class
+ *                 0 = decode path (own q_seq_len < LORA_TC_MIN_QLEN), 1 = tensor
+ *   seg_off[2*(N+1)]  first perm position of each (class, slot); [c*(N+1)+N] is
+ *                 the end of class c
+ *   dec_work[][4] {slot, perm_begin, perm_end, 0}: each class-0 slot run cut
+ *                 into runs of <= LORA_DEC_GROUP_ROWS rows
+ *   tc_work[][4]  {slot, row_begin, row_end, seq}: each class-1 sequence cut
+ *                 into tiles of <= LORA_TC_TILE_ROWS rows, sequences in perm order
+ *   counts[4]     {active rows, class-0 rows, #dec_work, #tc_work}
+ * A prompt chunk therefore uses one slot for all its rows, and a tile never
+ * crosses a sequence (TensorFold PR #47).  On a device-detected error every
+ * count is 0, so a following apply does nothing.
+ */
+
+/* Bytes of device workspace for up to max_seqs sequences, max_tokens rows and num_slots slots. */
+size_t lora_segments_bytes(int max_seqs, int max_tokens, int num_slots);
+
+/* Create a segments descriptor over caller workspace dev_ws (256-byte aligned). */
+int lora_segments_create(lora_segments** out, void* dev_ws, size_t ws_bytes, int max_seqs,
+                         int max_tokens, int num_slots);
+
+/* Build the metadata of one step on `stream` (one kernel, one CTA).
+ *   adapter_ids[num_seqs], q_seq_lens[num_seqs]: device int32.
+ * num_seqs = 0 (with num_tokens = 0) is a no-op step: no kernel is launched
+ * and the counts read as 0; num_seqs = 0 with num_tokens > 0 is LORA_ERR_SHAPE.  Device-detected errors: LORA_ERR_META if a length is negative or
+ * the lengths do not sum to num_tokens (checked first), LORA_ERR_SLOT if an id
+ * is outside [0, num_slots).  Host errors: LORA_ERR_ARG, LORA_ERR_SHAPE. */
+int lora_build_segments(lora_segments* seg, const int32_t* adapter_ids, const int32_t* q_seq_lens,
+                        int num_seqs, int num_tokens, lora_stream_t stream);
+
+/* Capacities of the work lists of this descriptor (host, no GPU work). */
+int lora_segments_capacity(const lora_segments* seg, int* dec_work_cap, int* tc_work_cap);
+
+/* Copy the metadata of the last build to host buffers (tests and tools; this
+ * synchronises `stream`).  Sizes: host_slot[T], host_perm[T], host_seg_off[2*(N+1)],
+ * host_counts[4], host_dec_work[4*dec_work_cap], host_tc_work[4*tc_work_cap]; any may be NULL. */
+int lora_segments_read(const lora_segments* seg, int32_t* host_slot, int32_t* host_perm,
+                       int32_t* host_seg_off, int32_t* host_counts, int32_t* host_dec_work,
+                       int32_t* host_tc_work, lora_stream_t stream);
+
+/* Read the status word (copies 4 bytes and synchronises `stream`). */
+int lora_get_status(const lora_segments* seg, int32_t* host_status, lora_stream_t stream);
+
+/* Reset the status word to LORA_OK on `stream`. */
+int lora_clear_status(lora_segments* seg, lora_stream_t stream);
+
+int lora_segments_destroy(lora_segments* seg);
+
+/* ----------------------------------------------------------------- apply --
+ * y += delta for every active row of the last lora_build_segments on `seg`:
+ *   x: device bf16 [T][ldx] (ldx >= d_in, ldx % 8 == 0, 16-byte aligned)
+ *   y: device fp32 [T][ldy] (ldy >= sum of lane_d_out, ldy % 4 == 0, 16-byte
+ *      aligned), updated in place; lane l occupies columns
+ *      [off_l, off_l + lane_d_out[l]), off_l = sum of the earlier lanes' widths.
+ * Rows of slot 0, and lanes of rank 0, are neither read nor written.  Each
+ * row's result depends only on its own x row, its adapter's factors and its
+ * own sequence's length: sums run in fp32 in a fixed order (decode path:
+ * shrink over d_in in fixed 2048-wide chunks reduced by a fixed tree, expand
+ * over the rank in ascending order, y = fma(scale, v, y); tensor path: tcgen05
+ * bf16 MMAs with fp32 accumulation, the rank-space vector split into two bf16
+ * halves for the expand, y = y + scale * v).
+ * If the step has no rows, or the pool has no loaded lane, nothing is
+ * launched.  Errors: LORA_ERR_ARG, LORA_ERR_SHAPE, LORA_ERR_CUDA; device
+ * timeouts set LORA_ERR_TIMEOUT in the segments' status word. */
+int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, const void* x,
+                             float* y, int64_t ldx, int64_t ldy, lora_stream_t stream);
+
+/* One kernel of lora_apply_shrink_expand, for per-kernel timing:
+ * stage 1 = decode shrink, 2 = decode expand, 3 = tensor shrink, 4 = tensor
+ * expand.  Running stages 1..4 in order is exactly lora_apply_shrink_expand. */
+int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y,
+                     int64_t ldx, int64_t ldy, int stage, lora_stream_t stream);
+
+/* ----------------------------------------------------------------- misc -- */
+
+/* Text of a status code. */
+const char* lora_status_string(int status);
+
+/* Kernels this library has launched in this process (all entry points). */
+uint64_t lora_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_DELTA_H */

@@ -1,0 +1,293 @@
+"""The delta on the GPU against the oracle, the closed forms and the
+batch-invariance properties.  Tolerance on the delta: |gpu - oracle| <=
+1e-3 + 1e-2 * |oracle| per element; untouched rows and invariances are
+bit-exact."""
+import numpy as np
+import pytest
+
+from adapter_gemv_lora_gb300 import workloads as W
+import lora_testlib as TL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from adapter_gemv_lora_gb300 import build
+    build.build()
+
+
+def _oracle_check(oracle_mod, wl, proj, rows=None, x=None, y0=None, what=""):
+    x = proj.x if x is None else x
+    y0 = proj.y0 if y0 is None else y0
+    slot = wl.per_token_slot()
+    y = TL.run_gpu(proj, wl.adapter_ids, wl.q_seq_lens, x=x, y0=y0)
+    if rows is None:
+        rows = np.arange(wl.T)
+    _, dref = oracle_mod.delta(proj, slot, rows=rows, x=x, y0=y0)
+    TL.assert_delta_close(y[rows], y0[rows], dref, what or wl.name)
+    TL.assert_rows_untouched(y, y0, np.nonzero(slot == 0)[0])
+    return y
+
+
+def _mixed_workload(seed=0, lanes=(256, 128), ranks=(16, 32, 8, 24)):
+    # decode rows, short and long prefill chunks (ragged tiles), base rows,
+    # heterogeneous ranks including ranks that are not multiples of 16
+    lens = [300, 1, 1, 64, 129, 5, 200, 63, 1, 1, 256, 2]
+    ids = [1, 2, 0, 3, 4, 1, 2, 4, 3, 0, 0, 1]
+    N, L = 5, len(lanes)
+    rank = np.zeros((N, L), dtype=np.int32)
+    for k in range(1, N):
+        rank[k, :] = ranks[(k - 1) % len(ranks)]
+    return W.custom_workload(lens, ids, d_in=512, lane_d_out=list(lanes), num_slots=N, max_rank=32,
+                             rank=rank, seed=seed)
+
+
+def test_mixed_small_full_oracle(oracle_mod):
+    wl = _mixed_workload()
+    _oracle_check(oracle_mod, wl, wl.projections[0], what="mixed")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_oproj"])
+def test_decode_configs_full(oracle_mod, name):
+    wl = W.make_workload(name)
+    _oracle_check(oracle_mod, wl, wl.projections[0])
+
+
+def test_mlp_decode_full(oracle_mod):
+    wl = W.make_workload("mlp_decode")
+    for proj in wl.projections:
+        _oracle_check(oracle_mod, wl, proj, what=proj.name)
+
+
+def _sample_rows(wl, n, seed=0):
+    rng = np.random.default_rng(seed)
+    starts = np.concatenate([[0], np.cumsum(wl.q_seq_lens)])
+    must = []
+    for s in range(wl.S):
+        b, e = int(starts[s]), int(starts[s + 1])
+        if e > b:
+            must += [b, e - 1] + [r for r in range(b, e, 128)] + [min(e - 1, r + 127) for r in range(b, e, 128)]
+    extra = rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist()
+    return np.unique(np.array(must + extra, dtype=np.int64))
+
+
+@pytest.mark.parametrize("name", ["prefill_qkv", "cont_batch"])
+def test_large_configs_sampled(oracle_mod, name):
+    wl = W.make_workload(name)
+    proj = wl.projections[0]
+    rows = _sample_rows(wl, 512)
+    _oracle_check(oracle_mod, wl, proj, rows=rows)
+
+
+def test_sentinels_in_base_rows_are_not_read_or_written(oracle_mod):
+    wl = _mixed_workload(seed=3)
+    proj = wl.projections[0]
+    slot = wl.per_token_slot()
+    x = proj.x.copy()
+    y0 = proj.y0.copy()
+    base = slot == 0
+    x[base] = TL.SENTINEL_X_BITS
+    y0.view(np.uint32)[base] = TL.SENTINEL_NAN_BITS
+    y = _oracle_check(oracle_mod, wl, proj, rows=np.nonzero(~base)[0], x=x, y0=y0)
+    assert np.all(y.view(np.uint32)[base] == TL.SENTINEL_NAN_BITS)
+
+
+def test_rank_zero_lane_is_not_written():
+    lens, ids = [1, 1, 200, 1], [1, 2, 1, 2]
+    rank = np.array([[0, 0, 0], [16, 0, 16], [0, 16, 0]], dtype=np.int32)
+    wl = W.custom_workload(lens, ids, d_in=256, lane_d_out=[128, 64, 64], num_slots=3, max_rank=16, rank=rank)
+    proj = wl.projections[0]
+    y = TL.run_gpu(proj, ids, lens)
+    slot = wl.per_token_slot()
+    off = [0, 128, 192, 256]
+    for t in range(wl.T):
+        for l in range(3):
+            a = y[t, off[l]:off[l + 1]].view(np.uint32)
+            b = proj.y0[t, off[l]:off[l + 1]].view(np.uint32)
+            assert np.array_equal(a, b) == (rank[slot[t], l] == 0)
+
+
+def test_scale_zero_leaves_y_bit_identical():
+    wl = _mixed_workload(seed=4)
+    proj = wl.projections[0]
+    proj.scale[:] = 0.0
+    y = TL.run_gpu(proj, wl.adapter_ids, wl.q_seq_lens)
+    assert np.array_equal(y.view(np.uint32), proj.y0.view(np.uint32))
+
+
+@pytest.mark.parametrize("qlen", [1, 200])
+def test_rank1_unit_vectors_closed_form(qlen):
+    # A = e_i^T, B = e_j, scale 2 (a power of two): y[t][j] = fl(y0 + 2 * x[t][i]) exactly.
+    d_in, d_out, i, j = 256, 128, 77, 5
+    wl = W.custom_workload([qlen, qlen], [1, 0], d_in=d_in, lane_d_out=[d_out], num_slots=2, max_rank=16,
+                           rank=np.array([[0], [1]]), alpha=np.array([[0.0], [2.0]]))
+    proj = wl.projections[0]
+    a = np.zeros((1, d_in), dtype=np.float32)
+    a[0, i] = 1
+    b = np.zeros((d_out, 1), dtype=np.float32)
+    b[j, 0] = 1
+    proj.A[1][0], proj.B[1][0] = W.bf16_bits(a), W.bf16_bits(b)
+    y = TL.run_gpu(proj, wl.adapter_ids, wl.q_seq_lens)
+    xf = W.bf16_bits_to_f32(proj.x)
+    exp = proj.y0.copy()
+    exp[:qlen, j] = proj.y0[:qlen, j] + np.float32(2.0) * xf[:qlen, i]
+    assert np.array_equal(y.view(np.uint32), exp.view(np.uint32))
+
+
+def test_linearity_doubling_x_doubles_y_from_zero():
+    wl = _mixed_workload(seed=5)
+    proj = wl.projections[0]
+    y0 = np.zeros_like(proj.y0)
+    y1 = TL.run_gpu(proj, wl.adapter_ids, wl.q_seq_lens, y0=y0)
+    x2 = W.bf16_bits(2.0 * W.bf16_bits_to_f32(proj.x))
+    y2 = TL.run_gpu(proj, wl.adapter_ids, wl.q_seq_lens, x=x2, y0=y0)
+    assert np.array_equal(y2, 2.0 * y1)
+
+
+def _seq_rows(lens):
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    return [np.arange(starts[s], starts[s + 1]) for s in range(len(lens))]
+
+
+def test_batch_composition_invariance():
+    # The same sequences (x rows, slot, own length) inside different batches
+    # give bit-identical rows.
+    base = _mixed_workload(seed=6)
+    proj = base.projections[0]
+    lens, ids = list(base.q_seq_lens), list(base.adapter_ids)
+    y_full = TL.run_gpu(proj, ids, lens)
+    rows = _seq_rows(lens)
+    rng = np.random.default_rng(0)
+    for trial in range(3):
+        keep = sorted(rng.choice(len(lens), size=6, replace=False).tolist())
+        # add foreign sequences with other slots between them
+        extra_lens = [1, 70, 1]
+        extra_ids = [4, 3, 2]
+        new_lens, new_ids, xs, ys, where = [], [], [], [], []
+        rng2 = np.random.default_rng(trial)
+        for n, s in enumerate(keep):
+            if n == 1:
+                for el, ei in zip(extra_lens, extra_ids):
+                    new_lens.append(el)
+                    new_ids.append(ei)
+                    xs.append(W.bf16_bits(rng2.standard_normal((el, proj.d_in)).astype(np.float32)))
+                    ys.append(rng2.standard_normal((el, proj.D)).astype(np.float32))
+                    where.append(None)
+            new_lens.append(lens[s])
+            new_ids.append(ids[s])
+            xs.append(proj.x[rows[s]])
+            ys.append(proj.y0[rows[s]])
+            where.append(s)
+        x = np.concatenate(xs)
+        y0 = np.concatenate(ys)
+        y = TL.run_gpu(proj, new_ids, new_lens, x=x, y0=y0, pool=TL.build_pool(proj, x.shape[0]))
+        for r, s in zip(_seq_rows(new_lens), where):
+            if s is not None:
+                assert np.array_equal(y[r].view(np.uint32), y_full[rows[s]].view(np.uint32)), (trial, s)
+
+
+def test_padding_and_slot_relabel_invariance():
+    wl = _mixed_workload(seed=7)
+    proj = wl.projections[0]
+    ids, lens = wl.adapter_ids, wl.q_seq_lens
+    y_a = TL.run_gpu(proj, ids, lens)
+    pool_b = TL.build_pool(proj, wl.T, max_rank=128)              # wider padding, same adapters
+    y_b = TL.run_gpu(proj, ids, lens, pool=pool_b)
+    assert np.array_equal(y_a.view(np.uint32), y_b.view(np.uint32))
+    relabel = {1: 7, 2: 3, 3: 5, 4: 1}
+    pool_c = TL.build_pool(proj, wl.T, slot_map=relabel)
+    ids_c = np.array([relabel.get(int(k), 0) for k in ids], dtype=np.int32)
+    y_c = TL.run_gpu(proj, ids_c, lens, pool=pool_c)
+    assert np.array_equal(y_a.view(np.uint32), y_c.view(np.uint32))
+
+
+def test_fused_lanes_equal_single_lane_pools(oracle_mod):
+    wl = _mixed_workload(seed=8, lanes=(256, 128, 128))
+    proj = wl.projections[0]
+    y = TL.run_gpu(proj, wl.adapter_ids, wl.q_seq_lens)
+    off = [0, 256, 384, 512]
+    for l in range(3):
+        single = W.Projection("lane", proj.d_in, [proj.lane_d_out[l]], proj.rank[:, l:l + 1].copy(),
+                              proj.scale[:, l:l + 1].copy(),
+                              [[proj.A[k][l]] for k in range(proj.rank.shape[0])],
+                              [[proj.B[k][l]] for k in range(proj.rank.shape[0])],
+                              proj.x, np.ascontiguousarray(proj.y0[:, off[l]:off[l + 1]]), proj.max_rank)
+        ys = TL.run_gpu(single, wl.adapter_ids, wl.q_seq_lens)
+        assert np.array_equal(ys.view(np.uint32), np.ascontiguousarray(y[:, off[l]:off[l + 1]]).view(np.uint32))
+
+
+def test_empty_and_all_base_batches():
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    wl = _mixed_workload(seed=9)
+    proj = wl.projections[0]
+    pool = TL.build_pool(proj, 1024)
+    seg = LD.LoraSegments(16, 1024, pool.num_slots)
+    x = torch.zeros((4, proj.d_in), dtype=torch.int16, device="cuda")
+    y = torch.randn((4, proj.D), device="cuda")
+    y_before = y.clone()
+    empty = torch.zeros(0, dtype=torch.int32, device="cuda")
+    n0 = LD.lora_launch_count()
+    seg.build(empty, empty, num_tokens=0)
+    LD.apply(pool, seg, x, y)
+    torch.cuda.synchronize()
+    assert LD.lora_launch_count() == n0          # an empty step launches nothing
+    assert seg.status() == 0
+    seg.build(torch.zeros(2, dtype=torch.int32, device="cuda"),
+              torch.tensor([3, 1], dtype=torch.int32, device="cuda"))
+    LD.apply(pool, seg, x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), y_before.view(torch.int32))
+    # a pool with no loaded adapter launches nothing
+    empty_pool = LD.LoraPool(pool.num_slots, 16, proj.d_in, proj.lane_d_out, 1024)
+    seg.build(torch.tensor([1, 2], dtype=torch.int32, device="cuda"),
+              torch.tensor([3, 1], dtype=torch.int32, device="cuda"))
+    n1 = LD.lora_launch_count()
+    LD.apply(empty_pool, seg, x, y)
+    torch.cuda.synchronize()
+    assert LD.lora_launch_count() == n1
+    assert torch.equal(y.view(torch.int32), y_before.view(torch.int32))
+
+
+def test_bad_metadata_makes_apply_a_noop():
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    wl = _mixed_workload(seed=10)
+    proj = wl.projections[0]
+    pool = TL.build_pool(proj, 64)
+    seg = LD.LoraSegments(8, 64, pool.num_slots)
+    x = TL.to_dev_u16(proj.x[:4])
+    y = torch.randn((4, proj.D), device="cuda")
+    y_before = y.clone()
+    seg.build(torch.tensor([1, 9], dtype=torch.int32, device="cuda"),
+              torch.tensor([2, 2], dtype=torch.int32, device="cuda"))
+    LD.apply(pool, seg, x, y)
+    torch.cuda.synchronize()
+    assert seg.status() == LD.LORA_ERR_SLOT
+    assert torch.equal(y.view(torch.int32), y_before.view(torch.int32))
+    seg.build(torch.tensor([1, 1], dtype=torch.int32, device="cuda"),
+              torch.tensor([2, 3], dtype=torch.int32, device="cuda"), num_tokens=4)
+    LD.apply(pool, seg, x, y)
+    torch.cuda.synchronize()
+    assert seg.status() == LD.LORA_ERR_META
+    assert torch.equal(y.view(torch.int32), y_before.view(torch.int32))
+
+
+def test_host_argument_checks():
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    wl = _mixed_workload(seed=11)
+    proj = wl.projections[0]
+    pool = TL.build_pool(proj, 64)
+    seg = TL.build_segments([1], [4], pool.num_slots, max_tokens=64)
+    x = torch.zeros((4, proj.d_in), dtype=torch.int16, device="cuda")
+    y = torch.zeros((4, proj.D), device="cuda")
+    with pytest.raises(LD.LoraError):       # ldx below d_in
+        LD.lora_apply_shrink_expand(pool.handle, seg.handle, x.data_ptr(), y.data_ptr(), 8, proj.D)
+    with pytest.raises(LD.LoraError):       # misaligned y
+        LD.lora_apply_shrink_expand(pool.handle, seg.handle, x.data_ptr(), y.data_ptr() + 4, proj.d_in, proj.D)
+    with pytest.raises(LD.LoraError):       # slot 0 cannot be loaded
+        LD.lora_pool_load(pool.handle, 0, 0, 4, 1.0, x.data_ptr(), x.data_ptr())
+    with pytest.raises(LD.LoraError):       # rank above max_rank
+        LD.lora_pool_load(pool.handle, 1, 0, 64, 1.0, x.data_ptr(), x.data_ptr())

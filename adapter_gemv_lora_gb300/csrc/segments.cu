@@ -284,7 +284,9 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   }
 }
 
-size_t seg_smem_bytes(int N) { return sizeof(int) * (size_t)(9 * N + 2); }
+// Dynamic shared memory of seg_build_kernel: cnt_tok, tok_off, run_tok (2N
+// each), cnt_tile (N), tc_base (N+1), run_tile (N), dec_base (N+1).
+size_t seg_smem_bytes(int N) { return sizeof(int) * (size_t)(3 * 2 * N + N + (N + 1) + N + (N + 1)); }
 
 }  // namespace
 

@@ -60,6 +60,7 @@ def load_library(path: str = LIB_PATH):
         "lora_segments_destroy": (I, [P]),
         "lora_apply_shrink_expand": (I, [P, P, P, P, I64, I64, P]),
         "lora_apply_stage": (I, [P, P, P, P, I64, I64, I, P]),
+        "lora_apply_shrink_expand_noalloc": (I, [P, P, P, P, I64, I64, P]),
         "lora_status_string": (ctypes.c_char_p, [I]),
         "lora_launch_count": (ctypes.c_uint64, []),
     }
@@ -172,6 +173,14 @@ def lora_segments_destroy(seg: int) -> None:
 
 def lora_apply_shrink_expand(pool: int, seg: int, x: int, y: int, ldx: int, ldy: int, stream: int = 0) -> None:
     _check(load_library().lora_apply_shrink_expand(pool, seg, x, y, ldx, ldy, stream), "lora_apply_shrink_expand")
+
+
+def lora_apply_shrink_expand_noalloc(pool: int, seg: int, x: int, y: int, ldx: int, ldy: int,
+                                     stream: int = 0) -> None:
+    """lora_apply_shrink_expand with the rank-space scratch in the library's
+    fixed device array instead of the pool, for callers that cannot allocate."""
+    _check(load_library().lora_apply_shrink_expand_noalloc(pool, seg, x, y, ldx, ldy, stream),
+           "lora_apply_shrink_expand_noalloc")
 
 
 def lora_apply_stage(pool: int, seg: int, x: int, y: int, ldx: int, ldy: int, stage: int, stream: int = 0) -> None:

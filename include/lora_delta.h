@@ -193,6 +193,30 @@ int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, co
 int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y,
                      int64_t ldx, int64_t ldy, int stage, lora_stream_t stream);
 
+/* The same step as lora_apply_shrink_expand for callers that cannot allocate
+ * device memory when they run: a plugin or custom-op host that passes the op
+ * only its input and output buffers, or a serving loop whose memory plan is
+ * frozen after start-up.  No passage of the pages has a counterpart; this is a
+ * property of the library, not of the method.
+ *   - The rank-space intermediate (decode partial sums and tensor-path rank
+ *     rows, (C + 1) * T * num_lanes * R16 floats with C = ceil(d_in / chunk))
+ *     lives in a fixed array compiled into the library, of
+ *     LORA_NOALLOC_SCRATCH_BYTES; every GPU that loads the library holds it
+ *     until the process exits.  A step that needs more returns LORA_ERR_SHAPE
+ *     before anything is enqueued.
+ *   - The call allocates nothing.  Its first call on a device looks up the
+ *     array's device address (cudaGetSymbolAddress) with that device current;
+ *     make that first call before any stream capture.  The current device must
+ *     be the pool's device (else LORA_ERR_ARG).
+ *   - Every call shares the one array.  Each scratch word a call reads it has
+ *     written earlier in the same call, so nothing needs clearing, but calls
+ *     whose GPU work overlaps (other streams, other threads) race on it: order
+ *     them on one stream.
+ * Arguments, results and other errors are those of lora_apply_shrink_expand. */
+#define LORA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lora_segments* seg, const void* x,
+                                     float* y, int64_t ldx, int64_t ldy, lora_stream_t stream);
+
 /* ----------------------------------------------------------------- misc -- */
 
 /* Text of a status code. */

@@ -7,16 +7,22 @@
 //   expand  y[row][o] += scale[k][l] * sum_i B[k][l][o][i] * u[row][i]   the delta
 //           scale * B @ (A @ x); xLLM PR #2014, shrink then expand)
 //
+// Both kernels are HBM streams of factor rows: a producer warp copies the
+// slot's rank rows (A rows for the shrink, B^T rows for the expand; true rank
+// only, never the padding) with the TMA bulk-copy engine into a ring of
+// shared-memory stages, and the compute warps consume them with 128-bit
+// shared loads.  The group's x rows (shrink) or u vectors (expand) stay in
+// registers / shared memory for the whole stream.
+//
 // Fixed summation order, independent of the group a row lands in:
-//  * shrink: d_in is cut into 2048-wide chunks (one work item each).  Inside a
-//    chunk, lane `ln` of warp `w` owns the 8-element runs at
-//    k = 256*s + 8*ln (s = w, w+4, ...), accumulated in that order with fma;
-//    the 32 lanes are then combined by a fixed xor butterfly (16,8,4,2,1) and
-//    the 4 warps left to right.  The chunks' partial sums go to the pool's
-//    scratch and are added in chunk order by the expand kernel.
-//  * expand: u is summed over chunks in order, then v[o] accumulates
-//    B[o][i] * u[i] for i = 0..r-1 in order with fma, and y = fma(scale, v, y).
-// Only true-rank rows of A and B^T are read; the padding never is.
+//  * shrink: d_in is cut into 1024-wide chunks (one work item each).  Inside a
+//    chunk lane `ln` of warp `w` owns the 8 elements at k = 256*w + 8*ln,
+//    accumulated in order with fma; the 32 lanes are combined by a fixed xor
+//    butterfly (16,8,4,2,1) and the 4 warps left to right.  The chunks'
+//    partial sums go to the pool's scratch and the expand kernel adds them in
+//    chunk order.
+//  * expand: u is the in-order sum of the chunk partials; v[o] accumulates
+//    B[o][i] * u[i] for i = 0..r-1 in order with fma; y = fma(scale, v, y).
 #include <cuda_runtime.h>
 
 #include "device.cuh"
@@ -25,13 +31,29 @@
 namespace lora {
 namespace {
 
+constexpr int kShWarps = 4;                      // shrink compute warps (256 k each)
+constexpr int kShThreads = (kShWarps + 1) * 32;  // + 1 producer warp
+constexpr int kShRows = 8;                       // rank rows per ring stage
+constexpr int kShStages = 4;
+constexpr int kShMaxRb = 128 / kShRows;          // rank blocks for r <= 128
+constexpr size_t kShRingBytes = (size_t)kShStages * kShRows * kDecKChunk * 2;  // 64 KB
+constexpr size_t kShRedBytes = (size_t)kShWarps * kShMaxRb * 64 * 4;          // 16 KB
+static_assert(kShWarps * 256 == kDecKChunk, "one 8-element slice per lane covers a chunk");
+
+constexpr int kExWarps = 4;                      // expand compute warps (8 columns per thread)
+constexpr int kExThreads = (kExWarps + 1) * 32;
+constexpr int kExRows = 16;                      // rank rows per ring stage
+constexpr int kExStages = 3;
+constexpr size_t kExRingBytes = (size_t)kExStages * kExRows * kDecNChunk * 2;  // 96 KB
+static_assert(kExWarps * 32 * 8 == kDecNChunk, "8 columns per thread cover a chunk");
+
 struct DecParams {
-  const int32_t* status;
   const int32_t* counts;
   const int4* work;
   const int32_t* perm;
   const int32_t* rank_tab;
   const float* scale_tab;
+  int32_t* status;
   const uint16_t* A[LORA_MAX_LANES];
   const uint16_t* Bt[LORA_MAX_LANES];
   float* u_dec;
@@ -57,55 +79,98 @@ __device__ __forceinline__ void rs_step(float* v, int lane, int o) {
   }
 }
 
-__global__ void __launch_bounds__(kDecThreads) dec_shrink_kernel(DecParams p) {
-  __shared__ __align__(16) uint16_t xs[kDecGroup][kDecKChunk];  // 32 KB
-  __shared__ float red[4][64];
+__global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* ring = reinterpret_cast<uint16_t*>(smem);         // [stage][row][kDecKChunk]
+  float* red = reinterpret_cast<float*>(smem + kShRingBytes);  // [warp][rank block][64]
+  __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages];
+  __shared__ int fail_sh;
+
   if (*p.status != 0) return;
   const int per_group = p.L * p.C;
   const int n_items = p.counts[2] * per_group;
+  if ((int)blockIdx.x >= n_items) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int w = item / per_group;
-    const int rem = item - w * per_group;
-    const int l = rem / p.C, c = rem - (rem / p.C) * p.C;
-    const int4 g = p.work[w];
-    const int k = g.x, p0 = g.y, nrows = g.z - g.y;
-    const int r = p.rank_tab[k * p.L + l];
-    if (r <= 0) continue;
-    const int k0 = c * kDecKChunk;
-    const int klen = min(kDecKChunk, p.d_in - k0);
-    const int nvec = klen >> 3;
-    __syncthreads();  // xs / red of the previous item are no longer read
-    for (int idx = tid; idx < kDecGroup * nvec; idx += kDecThreads) {
-      const int gg = idx / nvec, v = idx - gg * nvec;
-      uint4 q = make_uint4(0u, 0u, 0u, 0u);
-      if (gg < nrows) {
-        const int t = p.perm[p0 + gg];
-        q = ldg_nc_v4(p.x + (size_t)t * p.ldx + k0 + 8 * v);
-      }
-      *reinterpret_cast<uint4*>(&xs[gg][8 * v]) = q;
+  if (tid == 0) {
+    for (int s = 0; s < kShStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kShWarps);
     }
-    __syncthreads();
-    const uint16_t* Ab = p.A[l] + (size_t)k * p.R16 * p.d_in + k0;
-    const int nseg = (klen + 255) >> 8;
-    for (int rb = 0; rb < r; rb += 8) {
-      float acc[kDecGroup * 8];  // index gg*8 + i
-#pragma unroll
-      for (int j = 0; j < kDecGroup * 8; ++j) acc[j] = 0.f;
-      for (int s = warp; s < nseg; s += 4) {
-        const int kk = 256 * s + 8 * lane;
-        if (kk < klen) {
-          float xv[kDecGroup][8];
-#pragma unroll
-          for (int gg = 0; gg < kDecGroup; ++gg) {
-            const uint4 q = *reinterpret_cast<const uint4*>(&xs[gg][kk]);
-            unpack8(q, xv[gg]);
+    fail_sh = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kShWarps) {
+    // ---------------- producer: stream the slot's A rows of this chunk
+    if (lane == 0) {
+      uint32_t fill = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int w = item / per_group, rem = item - w * per_group;
+        const int l = rem / p.C, c = rem - l * p.C;
+        const int k = p.work[w].x;
+        const int r = p.rank_tab[k * p.L + l];
+        if (r <= 0) continue;
+        const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
+        const uint16_t* Ab = p.A[l] + (size_t)k * p.R16 * p.d_in + k0;
+        for (int rb = 0; rb < r; rb += kShRows, ++fill) {
+          const int s = fill % kShStages;
+          if (fill >= kShStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kShStages) - 1) & 1, &fail_sh)) {
+            ok = false;
+            fail_sh = 1;
+            break;
           }
+          const int rows = min(kShRows, r - rb);
+          mbar_expect_tx(&full_bar[s], (uint32_t)(rows * klen * 2));
+          for (int i = 0; i < rows; ++i)
+            bulk_load(ring + ((size_t)s * kShRows + i) * kDecKChunk, Ab + (size_t)(rb + i) * p.d_in,
+                      (uint32_t)(klen * 2), &full_bar[s]);
+        }
+      }
+    }
+  } else {
+    // ---------------- compute warps
+    uint32_t use = 0;
+    bool ok = true;
+    const int kk = warp * 256 + lane * 8;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const int w = item / per_group, rem = item - w * per_group;
+      const int l = rem / p.C, c = rem - l * p.C;
+      const int4 g = p.work[w];
+      const int k = g.x, p0 = g.y, nrows = g.z - g.y;
+      const int r = p.rank_tab[k * p.L + l];
+      if (r <= 0) continue;
+      const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
+      const bool has_k = kk < klen;
+      float xv[kDecGroup][8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (rb + i < r) {
+      for (int gg = 0; gg < kDecGroup; ++gg) {
+        if (gg < nrows && has_k) {
+          const int t = p.perm[p0 + gg];
+          unpack8(ldg_nc_v4(p.x + (size_t)t * p.ldx + k0 + kk), xv[gg]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) xv[gg][e] = 0.f;
+        }
+      }
+      const int nrb = (r + kShRows - 1) / kShRows;
+      for (int rb = 0; rb < nrb; ++rb, ++use) {
+        const int s = use % kShStages;
+        if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kShStages) & 1, &fail_sh)) {
+          ok = false;
+          fail_sh = 1;
+        }
+        float acc[kDecGroup * 8];  // index gg*8 + i
+#pragma unroll
+        for (int j = 0; j < kDecGroup * 8; ++j) acc[j] = 0.f;
+        if (ok && has_k) {
+          const uint16_t* st = ring + (size_t)s * kShRows * kDecKChunk + kk;
+#pragma unroll
+          for (int i = 0; i < kShRows; ++i) {
+            if (rb * kShRows + i < r) {
               float av[8];
-              unpack8(ldg_nc_v4(Ab + (size_t)(rb + i) * p.d_in + kk), av);
+              unpack8(*reinterpret_cast<const uint4*>(st + (size_t)i * kDecKChunk), av);
 #pragma unroll
               for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
@@ -113,118 +178,192 @@ __global__ void __launch_bounds__(kDecThreads) dec_shrink_kernel(DecParams p) {
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        rs_step<32>(acc, lane, 16);
+        rs_step<16>(acc, lane, 8);
+        rs_step<8>(acc, lane, 4);
+        rs_step<4>(acc, lane, 2);
+        rs_step<2>(acc, lane, 1);
+        // lane now holds the warp sums of values 2*lane and 2*lane+1
+        float* rw = red + ((size_t)warp * kShMaxRb + rb) * 64;
+        rw[2 * lane] = acc[0];
+        rw[2 * lane + 1] = acc[1];
       }
-      rs_step<32>(acc, lane, 16);
-      rs_step<16>(acc, lane, 8);
-      rs_step<8>(acc, lane, 4);
-      rs_step<4>(acc, lane, 2);
-      rs_step<2>(acc, lane, 1);
-      // lane now holds the warp sums of values 2*lane and 2*lane+1
-      red[warp][2 * lane] = acc[0];
-      red[warp][2 * lane + 1] = acc[1];
-      __syncthreads();
-      if (tid < 64) {
-        const int gg = tid >> 3, i = tid & 7;
-        if (gg < nrows && rb + i < r) {
-          float s = red[0][tid] + red[1][tid];
-          s += red[2][tid];
-          s += red[3][tid];
-          p.u_dec[(((size_t)c * p.max_tokens + p0 + gg) * p.L + l) * p.R16 + rb + i] = s;
+      named_bar_sync(1, kShWarps * 32);
+      for (int idx = tid; idx < nrb * 64; idx += kShWarps * 32) {
+        const int rb = idx >> 6, v = idx & 63, gg = v >> 3, i = v & 7;
+        if (gg < nrows && rb * kShRows + i < r) {
+          float sum = red[(size_t)rb * 64 + v];
+#pragma unroll
+          for (int ww = 1; ww < kShWarps; ++ww) sum += red[((size_t)ww * kShMaxRb + rb) * 64 + v];
+          p.u_dec[(((size_t)c * p.max_tokens + p0 + gg) * p.L + l) * p.R16 + rb * kShRows + i] = sum;
         }
       }
-      __syncthreads();
+      named_bar_sync(1, kShWarps * 32);
     }
   }
+  __syncthreads();
+  if (tid == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kDecThreads) dec_expand_kernel(DecParams p) {
-  __shared__ __align__(16) float us[128][kDecGroup];  // [rank][row]
+__global__ void __launch_bounds__(kExThreads) dec_expand_kernel(DecParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* ring = reinterpret_cast<uint16_t*>(smem);  // [stage][row][kDecNChunk]
+  __shared__ __align__(16) float us[128][kDecGroup];   // [rank][row]
+  __shared__ __align__(8) uint64_t full_bar[kExStages], empty_bar[kExStages];
+  __shared__ int fail_sh;
+
   if (*p.status != 0) return;
   const int total_nc = p.nc_base[p.L];
   const int n_items = p.counts[2] * total_nc;
-  const int tid = threadIdx.x;
+  if ((int)blockIdx.x >= n_items) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kExStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kExWarps);
+    }
+    fail_sh = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   const size_t cstride = (size_t)p.max_tokens * p.L * p.R16;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int w = item / total_nc;
-    const int q = item - w * total_nc;
-    int l = 0;
-    while (l + 1 < p.L && q >= p.nc_base[l + 1]) ++l;
-    const int j = q - p.nc_base[l];
-    const int4 g = p.work[w];
-    const int k = g.x, p0 = g.y, nrows = g.z - g.y;
-    const int r = p.rank_tab[k * p.L + l];
-    if (r <= 0) continue;
-    __syncthreads();  // us of the previous item are no longer read
-    for (int idx = tid; idx < r * kDecGroup; idx += kDecThreads) {
-      const int i = idx >> 3, gg = idx & 7;
-      float s = 0.f;
-      if (gg < nrows) {
-        const float* u = p.u_dec + ((size_t)(p0 + gg) * p.L + l) * p.R16 + i;
-        s = u[0];
-        for (int c = 1; c < p.C; ++c) s += u[c * cstride];
-      }
-      us[i][gg] = s;
-    }
-    __syncthreads();
-    const int dout = p.d_out[l];
-    const int o = j * kDecNChunk + 8 * tid;
-    if (o >= dout) continue;
-    float4 yv[kDecGroup][2];
-    float* yrow[kDecGroup];
-#pragma unroll
-    for (int gg = 0; gg < kDecGroup; ++gg) {
-      yrow[gg] = nullptr;
-      if (gg < nrows) {
-        const int t = p.perm[p0 + gg];
-        yrow[gg] = p.y + (size_t)t * p.ldy + p.off[l] + o;
-        yv[gg][0] = *reinterpret_cast<const float4*>(yrow[gg]);
-        yv[gg][1] = *reinterpret_cast<const float4*>(yrow[gg] + 4);
+
+  if (warp == kExWarps) {
+    // ---------------- producer: stream the slot's B^T rows of this column chunk
+    if (lane == 0) {
+      uint32_t fill = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int w = item / total_nc, q = item - w * total_nc;
+        int l = 0;
+        while (l + 1 < p.L && q >= p.nc_base[l + 1]) ++l;
+        const int n0 = (q - p.nc_base[l]) * kDecNChunk;
+        const int k = p.work[w].x;
+        const int r = p.rank_tab[k * p.L + l];
+        if (r <= 0) continue;
+        const int dout = p.d_out[l];
+        const int ncols = min(kDecNChunk, dout - n0);
+        const uint16_t* Bb = p.Bt[l] + (size_t)k * p.R16 * dout + n0;
+        for (int rb = 0; rb < r; rb += kExRows, ++fill) {
+          const int s = fill % kExStages;
+          if (fill >= kExStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kExStages) - 1) & 1, &fail_sh)) {
+            ok = false;
+            fail_sh = 1;
+            break;
+          }
+          const int rows = min(kExRows, r - rb);
+          mbar_expect_tx(&full_bar[s], (uint32_t)(rows * ncols * 2));
+          for (int i = 0; i < rows; ++i)
+            bulk_load(ring + ((size_t)s * kExRows + i) * kDecNChunk, Bb + (size_t)(rb + i) * dout,
+                      (uint32_t)(ncols * 2), &full_bar[s]);
+        }
       }
     }
-    float acc[kDecGroup][8];
+  } else {
+    // ---------------- compute warps: 8 output columns per thread
+    uint32_t use = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const int w = item / total_nc, q = item - w * total_nc;
+      int l = 0;
+      while (l + 1 < p.L && q >= p.nc_base[l + 1]) ++l;
+      const int n0 = (q - p.nc_base[l]) * kDecNChunk;
+      const int4 g = p.work[w];
+      const int k = g.x, p0 = g.y, nrows = g.z - g.y;
+      const int r = p.rank_tab[k * p.L + l];
+      if (r <= 0) continue;
+      const int dout = p.d_out[l];
+      named_bar_sync(1, kExWarps * 32);  // us of the previous item are no longer read
+      for (int idx = tid; idx < r * kDecGroup; idx += kExWarps * 32) {
+        const int i = idx >> 3, gg = idx & 7;
+        float s = 0.f;
+        if (gg < nrows) {
+          const float* u = p.u_dec + ((size_t)(p0 + gg) * p.L + l) * p.R16 + i;
+          s = u[0];
+          for (int c = 1; c < p.C; ++c) s += u[c * cstride];
+        }
+        us[i][gg] = s;
+      }
+      named_bar_sync(1, kExWarps * 32);
+      const int o = n0 + 8 * tid;
+      const bool has = o < dout;
+      float4 yv[kDecGroup][2];
+      float* yrow[kDecGroup];
 #pragma unroll
-    for (int gg = 0; gg < kDecGroup; ++gg)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[gg][e] = 0.f;
-    const uint16_t* Bb = p.Bt[l] + (size_t)k * p.R16 * dout + o;
-#pragma unroll 2
-    for (int i = 0; i < r; ++i) {
-      float bv[8];
-      unpack8(ldg_nc_v4(Bb + (size_t)i * dout), bv);
-      const float4 u0 = *reinterpret_cast<const float4*>(&us[i][0]);
-      const float4 u1 = *reinterpret_cast<const float4*>(&us[i][4]);
-      const float ug[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      for (int gg = 0; gg < kDecGroup; ++gg) {
+        yrow[gg] = nullptr;
+        if (has && gg < nrows) {
+          const int t = p.perm[p0 + gg];
+          yrow[gg] = p.y + (size_t)t * p.ldy + p.off[l] + o;
+          yv[gg][0] = *reinterpret_cast<const float4*>(yrow[gg]);
+          yv[gg][1] = *reinterpret_cast<const float4*>(yrow[gg] + 4);
+        }
+      }
+      float acc[kDecGroup][8];
 #pragma unroll
       for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[gg][e] = fmaf(bv[e], ug[gg], acc[gg][e]);
-    }
-    const float sc = p.scale_tab[k * p.L + l];
+        for (int e = 0; e < 8; ++e) acc[gg][e] = 0.f;
+      const int nrb = (r + kExRows - 1) / kExRows;
+      for (int rb = 0; rb < nrb; ++rb, ++use) {
+        const int s = use % kExStages;
+        if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kExStages) & 1, &fail_sh)) {
+          ok = false;
+          fail_sh = 1;
+        }
+        if (ok && has) {
+          const uint16_t* st = ring + (size_t)s * kExRows * kDecNChunk + 8 * tid;
+#pragma unroll 4
+          for (int i = 0; i < kExRows; ++i) {
+            const int ri = rb * kExRows + i;
+            if (ri < r) {
+              float bv[8];
+              unpack8(*reinterpret_cast<const uint4*>(st + (size_t)i * kDecNChunk), bv);
+              const float4 u0 = *reinterpret_cast<const float4*>(&us[ri][0]);
+              const float4 u1 = *reinterpret_cast<const float4*>(&us[ri][4]);
+              const float ug[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-    for (int gg = 0; gg < kDecGroup; ++gg) {
-      if (gg < nrows) {
-        float4 a = yv[gg][0], b = yv[gg][1];
-        a.x = fmaf(sc, acc[gg][0], a.x);
-        a.y = fmaf(sc, acc[gg][1], a.y);
-        a.z = fmaf(sc, acc[gg][2], a.z);
-        a.w = fmaf(sc, acc[gg][3], a.w);
-        b.x = fmaf(sc, acc[gg][4], b.x);
-        b.y = fmaf(sc, acc[gg][5], b.y);
-        b.z = fmaf(sc, acc[gg][6], b.z);
-        b.w = fmaf(sc, acc[gg][7], b.w);
-        *reinterpret_cast<float4*>(yrow[gg]) = a;
-        *reinterpret_cast<float4*>(yrow[gg] + 4) = b;
+              for (int gg = 0; gg < kDecGroup; ++gg)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[gg][e] = fmaf(bv[e], ug[gg], acc[gg][e]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+      if (!ok || !has) continue;
+      const float sc = p.scale_tab[k * p.L + l];
+#pragma unroll
+      for (int gg = 0; gg < kDecGroup; ++gg) {
+        if (gg < nrows) {
+          float4 a = yv[gg][0], b = yv[gg][1];
+          a.x = fmaf(sc, acc[gg][0], a.x);
+          a.y = fmaf(sc, acc[gg][1], a.y);
+          a.z = fmaf(sc, acc[gg][2], a.z);
+          a.w = fmaf(sc, acc[gg][3], a.w);
+          b.x = fmaf(sc, acc[gg][4], b.x);
+          b.y = fmaf(sc, acc[gg][5], b.y);
+          b.z = fmaf(sc, acc[gg][6], b.z);
+          b.w = fmaf(sc, acc[gg][7], b.w);
+          *reinterpret_cast<float4*>(yrow[gg]) = a;
+          *reinterpret_cast<float4*>(yrow[gg] + 4) = b;
+        }
       }
     }
   }
+  __syncthreads();
+  if (tid == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
 }
 
 DecParams make_params(const lora_pool* pool, const lora_segments* seg) {
   DecParams p{};
-  p.status = seg->status;
   p.counts = seg->counts;
   p.work = seg->dec_work;
   p.perm = seg->perm;
+  p.status = seg->status;
   p.rank_tab = pool->rank_tab;
   p.scale_tab = pool->scale_tab;
   for (int l = 0; l < LORA_MAX_LANES; ++l) {
@@ -259,10 +398,13 @@ int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uin
   p.x = x;
   p.ldx = ldx;
   const long long items = (long long)dec_group_bound(pool, seg) * pool->L * pool->C_dec;
-  const long long cap = 3LL * sm_count(pool->device);
+  const long long cap = 2LL * sm_count(pool->device);
   const int grid = (int)(items < cap ? items : cap);
   if (grid <= 0) return LORA_OK;
-  dec_shrink_kernel<<<grid, kDecThreads, 0, st>>>(p);
+  const int smem = (int)(kShRingBytes + kShRedBytes);
+  if (cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  dec_shrink_kernel<<<grid, kShThreads, smem, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
@@ -272,10 +414,13 @@ int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y,
   p.y = y;
   p.ldy = ldy;
   const long long items = (long long)dec_group_bound(pool, seg) * p.nc_base[pool->L];
-  const long long cap = 3LL * sm_count(pool->device);
+  const long long cap = 2LL * sm_count(pool->device);
   const int grid = (int)(items < cap ? items : cap);
   if (grid <= 0) return LORA_OK;
-  dec_expand_kernel<<<grid, kDecThreads, 0, st>>>(p);
+  const int smem = (int)kExRingBytes;
+  if (cudaFuncSetAttribute(dec_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  dec_expand_kernel<<<grid, kExThreads, smem, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }

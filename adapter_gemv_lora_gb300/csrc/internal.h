@@ -15,9 +15,8 @@ namespace lora {
 
 // Decode path tiling.
 constexpr int kDecGroup = LORA_DEC_GROUP_ROWS;  // rows of one slot per decode group
-constexpr int kDecKChunk = 2048;                // d_in elements per shrink item
+constexpr int kDecKChunk = 1024;                // d_in elements per shrink item
 constexpr int kDecNChunk = 1024;                // output columns per expand item
-constexpr int kDecThreads = 128;
 
 // Tensor path tiling.
 constexpr int kTcTile = LORA_TC_TILE_ROWS;  // MMA M
@@ -25,12 +24,22 @@ constexpr int kTcKBlock = 64;               // d_in elements per TMA stage (128 
 constexpr int kTcNT = 128;                  // expand MMA N per accumulator buffer
 constexpr int kTcNGroup = 1024;             // output columns per expand item
 constexpr int kTcThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kTcKSplit = 2;                // shrink K ranges per tile (fixed: sums stay row-local)
 
 inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
 inline int ceil_div(int v, int m) { return (v + m - 1) / m; }
 
 struct TmapLanes {
   CUtensorMap m[LORA_MAX_LANES];
+};
+
+// Tensor maps of one operand per lane in four box sizes: index s has a box of
+// 16 << s rank rows (A) or 1 << s groups of 16 rank columns (B), so a rank is
+// loaded with one TMA copy per set bit of r16 / 16.  Sizes above the pool's
+// R16 are left zeroed and never used.
+constexpr int kTmapSizes = 4;
+struct TmapSized {
+  CUtensorMap m[kTmapSizes][LORA_MAX_LANES];
 };
 
 }  // namespace lora
@@ -46,12 +55,13 @@ struct lora_pool {
   float* scale_tab = nullptr;       // [N][L]
   uint16_t* A[LORA_MAX_LANES] = {};   // per lane [N][R16][d_in]
   uint16_t* Bt[LORA_MAX_LANES] = {};  // per lane [N][R16][d_out]   (decode expand)
-  uint16_t* Bk[LORA_MAX_LANES] = {};  // per lane [N][d_out][R16]   (tensor expand, K-major)
+  uint16_t* Bk[LORA_MAX_LANES] = {};  // per lane [N][R16/16][d_out][16] (tensor expand: K-major
+                                      // groups of 16 rank columns, each group contiguous)
   float* u_dec = nullptr;           // [C_dec][max_tokens][L][R16] split-K partial sums
-  float* u_tc = nullptr;            // [max_tokens][L][R16]
+  float* u_tc = nullptr;            // [kTcKSplit][max_tokens][L][R16] partial sums over K ranges
   std::vector<int> h_rank;          // host mirror of rank_tab
-  lora::TmapLanes tm_a;             // A of each lane, 3-D {d_in, R16, N}, box {64,16,1}, SW128
-  lora::TmapLanes tm_bk;            // Bk of each lane, 3-D {R16, d_out, N}, box {16,128,1}, SW32
+  lora::TmapSized tm_a;             // A, 3-D {d_in, R16, N}, box {64, 16<<s, 1}, 128-byte swizzle
+  lora::TmapSized tm_bk;            // Bk, 3-D {16, d_out, R16/16*N}, box {16, 128, 1<<s}, 32-byte swizzle
 };
 
 struct lora_segments {

@@ -59,10 +59,10 @@ extern "C" int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lor
   if (T == 0 || !loaded) return LORA_OK;  // nothing to do: nothing is launched
 
   // Rank-space scratch this step needs: decode partials [C][T][L][R16] plus
-  // tensor-path rows [T][L][R16], fp32.
+  // tensor-path partial rows [kTcKSplit][T][L][R16], fp32.
   const size_t per_row = (size_t)pool->L * pool->R16;
   const size_t dec_floats = (size_t)pool->C_dec * T * per_row;
-  const size_t need = dec_floats + (size_t)T * per_row;
+  const size_t need = dec_floats + (size_t)lora::kTcKSplit * T * per_row;
   if (need > kScratchFloats) return LORA_ERR_SHAPE;
 
   int dev = -1;
@@ -83,7 +83,7 @@ extern "C" int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lor
   view.L = pool->L;
   view.D = pool->D;
   view.C_dec = pool->C_dec;
-  view.max_tokens = T;  // stride of the decode partials in the scratch
+  view.max_tokens = T;  // stride of the partial sums in the scratch
   for (int l = 0; l < LORA_MAX_LANES; ++l) {
     view.d_out[l] = pool->d_out[l];
     view.off[l] = pool->off[l];

@@ -11,10 +11,13 @@
 //   Bt_l      bf16  [N][R16][d_out_l]   per lane; B transposed, for the decode
 //                                       expand (each rank row is a contiguous
 //                                       run of output columns)
-//   Bk_l      bf16  [N][d_out_l][R16]   per lane; B as given (K-major rows of
-//                                       the rank), for the tensor-core expand
+//   Bk_l      bf16  [N][R16/16][d_out_l][16]  per lane; B as given, cut into
+//                                       groups of 16 rank columns (K-major), so
+//                                       one TMA box loads several whole groups
+//                                       for the tensor-core expand
 //   u_dec     f32   [C][max_tokens][L][R16]  decode split-K partial sums
-//   u_tc      f32   [max_tokens][L][R16]     tensor-path rank-space rows
+//   u_tc      f32   [2][max_tokens][L][R16]  tensor-path rank-space rows, one
+//                                            partial sum per half of d_in
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -40,7 +43,9 @@ __global__ void repack_kernel(const uint16_t* __restrict__ A, const uint16_t* __
     Bt[idx] = i < rank ? B[(size_t)o * rank + i] : (uint16_t)0;
   }
   for (size_t idx = tid; idx < nb; idx += stride) {
-    const int o = (int)(idx / R16), i = (int)(idx % R16);
+    const int q = (int)(idx / ((size_t)d_out * 16));
+    const int rem = (int)(idx % ((size_t)d_out * 16));
+    const int o = rem / 16, i = 16 * q + rem % 16;
     Bk[idx] = i < rank ? B[(size_t)o * rank + i] : (uint16_t)0;
   }
   if (tid == 0) {
@@ -80,7 +85,7 @@ bool pool_layout(int N, int R, int d_in, int L, const int* d_out, int max_tokens
     P->Bk[l] = o; o = align1k(o + 2 * (size_t)N * d_out[l] * R16);
   }
   P->u_dec = o; o = align1k(o + 4 * (size_t)P->C_dec * max_tokens * L * R16);
-  P->u_tc = o; o = align1k(o + 4 * (size_t)max_tokens * L * R16);
+  P->u_tc = o; o = align1k(o + 4 * (size_t)kTcKSplit * max_tokens * L * R16);
   P->total = o;
   return true;
 }
@@ -154,24 +159,26 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   std::memset(&p->tm_bk, 0, sizeof(p->tm_bk));
   for (int l = 0; l < num_lanes; ++l) {
     const uint64_t R16 = (uint64_t)P.R16;
-    {
-      const uint64_t dims[3] = {(uint64_t)d_in, R16, (uint64_t)num_slots};
-      const uint64_t strides[2] = {2ull * d_in, 2ull * d_in * R16};
-      const uint32_t box[3] = {(uint32_t)kTcKBlock, 16u, 1u};
-      if (!encode_tmap(&p->tm_a.m[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->A[l], dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_128B)) {
-        delete p;
-        return LORA_ERR_CUDA;
+    for (int sz = 0; sz < kTmapSizes; ++sz) {
+      if ((16u << sz) <= R16) {
+        const uint64_t dims[3] = {(uint64_t)d_in, R16, (uint64_t)num_slots};
+        const uint64_t strides[2] = {2ull * d_in, 2ull * d_in * R16};
+        const uint32_t box[3] = {(uint32_t)kTcKBlock, 16u << sz, 1u};
+        if (!encode_tmap(&p->tm_a.m[sz][l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->A[l], dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) {
+          delete p;
+          return LORA_ERR_CUDA;
+        }
       }
-    }
-    {
-      const uint64_t dims[3] = {R16, (uint64_t)lane_d_out[l], (uint64_t)num_slots};
-      const uint64_t strides[2] = {2ull * R16, 2ull * R16 * lane_d_out[l]};
-      const uint32_t box[3] = {16u, (uint32_t)kTcNT, 1u};
-      if (!encode_tmap(&p->tm_bk.m[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->Bk[l], dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_32B)) {
-        delete p;
-        return LORA_ERR_CUDA;
+      if ((1u << sz) <= R16 / 16) {
+        const uint64_t dims[3] = {16ull, (uint64_t)lane_d_out[l], (R16 / 16) * (uint64_t)num_slots};
+        const uint64_t strides[2] = {32ull, 32ull * lane_d_out[l]};
+        const uint32_t box[3] = {16u, (uint32_t)kTcNT, 1u << sz};
+        if (!encode_tmap(&p->tm_bk.m[sz][l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->Bk[l], dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_32B)) {
+          delete p;
+          return LORA_ERR_CUDA;
+        }
       }
     }
   }

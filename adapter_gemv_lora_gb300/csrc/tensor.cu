@@ -43,6 +43,7 @@ struct TcShrinkParams {
   float* u_tc;
   int32_t* status;
   int L, R16, num_kb, stages, stage_bytes, tmem_cols;
+  size_t u_split_stride;  // floats between the K-range partials of u_tc
 };
 
 struct TcExpandParams {
@@ -51,6 +52,7 @@ struct TcExpandParams {
   const int32_t* rank_tab;
   const float* scale_tab;
   const float* u_tc;
+  size_t u_split_stride;
   float* y;
   int32_t* status;
   int64_t ldy;
@@ -62,9 +64,9 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
-    tc_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ TmapLanes tm_a,
-                     TcShrinkParams p) {
+__global__ void __launch_bounds__(kTcThreads, 2)
+    tc_shrink_kernel(const __grid_constant__ CUtensorMap tm_x128, const __grid_constant__ CUtensorMap tm_x32,
+                     const __grid_constant__ TmapSized tm_a, TcShrinkParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -73,8 +75,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ int fail_sh;
 
   if (*p.status != 0) return;
-  const int tile = blockIdx.x;
+  // CTA = (tile, K range): the k-blocks of d_in are cut into kTcKSplit fixed
+  // ranges; each CTA sums one range and the expand adds the partials in order.
+  const int tile = blockIdx.x / kTcKSplit;
+  const int ksplit = blockIdx.x - tile * kTcKSplit;
   if (tile >= p.counts[3]) return;
+  const int kb_lo = ksplit * p.num_kb / kTcKSplit, kb_hi = (ksplit + 1) * p.num_kb / kTcKSplit;
+  const int nkb = kb_hi - kb_lo;
   const int4 wk = p.work[tile];
   const int k = wk.x, rb = wk.y, re = wk.z;
   int r16[LORA_MAX_LANES];
@@ -107,17 +114,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
+  // A full tile takes one 128-row X box per stage; the ragged last tile of a
+  // sequence takes 32-row boxes up to its end.
+  const bool full_tile = (re - rb) == kTcTile;
   const int nbox = (re - rb + kXBoxRows - 1) / kXBoxRows;
-  uint32_t tx_bytes = (uint32_t)nbox * kXBoxRows * kTcKBlock * 2;
+  uint32_t tx_bytes = (uint32_t)(full_tile ? kTcTile : nbox * kXBoxRows) * kTcKBlock * 2;
 #pragma unroll
   for (int l = 0; l < LORA_MAX_LANES; ++l) tx_bytes += (uint32_t)r16[l] * kTcKBlock * 2;
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        const int s = kb % p.stages;
-        if (kb >= p.stages) {
-          if (!mbar_wait_or_fail(&empty_bar[s], ((kb / p.stages) - 1) & 1, &fail_sh)) {
+      for (int kj = 0; kj < nkb; ++kj) {
+        const int kb = kb_lo + kj;
+        const int s = kj % p.stages;
+        if (kj >= p.stages) {
+          if (!mbar_wait_or_fail(&empty_bar[s], ((kj / p.stages) - 1) & 1, &fail_sh)) {
             fail_sh = 1;
             break;
           }
@@ -125,19 +136,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t* xs = smem + (size_t)s * p.stage_bytes;
         uint8_t* as = xs + kXStageBytes;
         mbar_expect_tx(&full_bar[s], tx_bytes);
-        for (int b = 0; b < nbox; ++b)
-          tma_load_2d(xs + b * kXBoxRows * kTcKBlock * 2, &tm_x, kb * kTcKBlock, rb + kXBoxRows * b, &full_bar[s]);
-#pragma unroll
-        for (int l = 0; l < LORA_MAX_LANES; ++l)
-          for (int q = 0; q < r16[l] / 16; ++q)
-            tma_load_3d(as + (size_t)(l * p.R16 + 16 * q) * kTcKBlock * 2, &tm_a.m[l], kb * kTcKBlock, 16 * q, k,
+        if (full_tile) {
+          tma_load_2d(xs, &tm_x128, kb * kTcKBlock, rb, &full_bar[s]);
+        } else {
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(xs + b * kXBoxRows * kTcKBlock * 2, &tm_x32, kb * kTcKBlock, rb + kXBoxRows * b,
                         &full_bar[s]);
+        }
+#pragma unroll
+        for (int l = 0; l < LORA_MAX_LANES; ++l) {
+          int row = 0;
+          for (int sz = kTmapSizes - 1; sz >= 0; --sz) {
+            const int rows = 16 << sz;
+            while (r16[l] - row >= rows) {
+              tma_load_3d(as + (size_t)(l * p.R16 + row) * kTcKBlock * 2, &tm_a.m[sz][l], kb * kTcKBlock, row, k,
+                          &full_bar[s]);
+              row += rows;
+            }
+          }
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % p.stages;
         if (!mbar_wait_or_fail(&full_bar[s], (kb / p.stages) & 1, &fail_sh)) {
           fail_sh = 1;
@@ -177,7 +200,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float v[16];
           tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(l * p.R16 + 16 * q), v);
           if (valid) {
-            float4* dst = reinterpret_cast<float4*>(p.u_tc + ((size_t)t * p.L + l) * p.R16 + 16 * q);
+            float4* dst = reinterpret_cast<float4*>(p.u_tc + ksplit * p.u_split_stride +
+                                                    ((size_t)t * p.L + l) * p.R16 + 16 * q);
             dst[0] = make_float4(v[0], v[1], v[2], v[3]);
             dst[1] = make_float4(v[4], v[5], v[6], v[7]);
             dst[2] = make_float4(v[8], v[9], v[10], v[11]);
@@ -196,11 +220,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
-    tc_expand_kernel(const __grid_constant__ TmapLanes tm_b, const __grid_constant__ CUtensorMap tm_y,
-                     TcExpandParams p) {
+// Expand CTA: warp 0 TMA, warp 1 MMA, warps 2-5 read TMEM (one lane quadrant
+// each) and stage scale * acc in shared memory, warps 6-13 do the y update with
+// coalesced 128-bit loads and stores (two 256-byte row segments per warp
+// instruction, the next half-chunk's y loads in flight while the current one
+// is added).  Rows past the end of the tile's sequence are skipped.
+constexpr int kExpTmemWarps = 4;
+constexpr int kExpRmwWarps = 16;
+constexpr int kExpThreads = (2 + kExpTmemWarps + kExpRmwWarps) * 32;
+constexpr int kHalfCols = 64;                          // columns per staged half chunk
+constexpr int kHalfBytes = kTcTile * kHalfCols * 4;    // 32 KB
+constexpr int kRmwRowsPerWarp = kTcTile / kExpRmwWarps;  // 16
+
+__global__ void __launch_bounds__(kExpThreads, 1)
+    tc_expand_kernel(const __grid_constant__ TmapSized tm_b, TcExpandParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bfull[2], bempty[2], afull[2], aempty[2];
+  __shared__ __align__(8) uint64_t bfull[2], bempty[2], afull[2], aempty[2], sfull[2], sempty[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int fail_sh;
 
@@ -223,10 +258,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nchunks = (n_end - n_begin + kTcNT - 1) / kTcNT;
   const float sc = p.scale_tab[k * p.L + l];
 
-  // shared memory: [y staging 4 warps x 2 x 4 KB][B stages 2 x R16*256][U hi 128*R16*2][U lo]
+  // shared memory: [y staging 2 x 32 KB][B stages 2 x R16*256][U hi 128*R16*2][U lo]
   uint8_t* smem = align1024(smem_raw);
   uint8_t* ystage = smem;
-  uint8_t* bst = smem + 32768;
+  uint8_t* bst = smem + 2 * kHalfBytes;
   const size_t bstage_bytes = (size_t)p.R16 * kTcNT * 2;
   uint8_t* uhi = bst + 2 * bstage_bytes;
   uint8_t* ulo = uhi + (size_t)kTcTile * p.R16 * 2;
@@ -238,7 +273,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bfull[s], 1);
       mbar_init(&bempty[s], 1);
       mbar_init(&afull[s], 1);
-      mbar_init(&aempty[s], 4);
+      mbar_init(&aempty[s], kExpTmemWarps);
+      mbar_init(&sfull[s], kExpTmemWarps);
+      mbar_init(&sempty[s], kExpRmwWarps);
     }
     fail_sh = 0;
     fence_mbar_init();
@@ -248,7 +285,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_relinquish();
   }
   // U rows -> bf16 hi / lo halves in the K-major core-matrix layout.
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 2 + kExpTmemWarps) {
     const int m = (warp & 3) * 32 + lane;
     const int t = rb + m;
     const bool valid = t < re;
@@ -259,6 +296,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float4 a = *reinterpret_cast<const float4*>(urow + 8 * kg);
         const float4 b = *reinterpret_cast<const float4*>(urow + 8 * kg + 4);
         u[0] = a.x; u[1] = a.y; u[2] = a.z; u[3] = a.w; u[4] = b.x; u[5] = b.y; u[6] = b.z; u[7] = b.w;
+#pragma unroll
+        for (int ks = 1; ks < kTcKSplit; ++ks) {  // K-range partials, in order
+          const float4 c = *reinterpret_cast<const float4*>(urow + ks * p.u_split_stride + 8 * kg);
+          const float4 d = *reinterpret_cast<const float4*>(urow + ks * p.u_split_stride + 8 * kg + 4);
+          u[0] += c.x; u[1] += c.y; u[2] += c.z; u[3] += c.w; u[4] += d.x; u[5] += d.y; u[6] += d.z; u[7] += d.w;
+        }
       } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) u[e] = 0.f;
@@ -296,8 +339,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mbar_expect_tx(&bfull[s], (uint32_t)nk * kTcNT * 32);
         uint8_t* bs = bst + (size_t)s * bstage_bytes;
-        for (int qq = 0; qq < nk; ++qq)
-          tma_load_3d(bs + (size_t)qq * kTcNT * 32, &tm_b.m[l], 16 * qq, n_begin + c * kTcNT, k, &bfull[s]);
+        // groups of 16 rank columns, several per copy: [group][128 rows][16]
+        int qq = 0;
+        for (int sz = kTmapSizes - 1; sz >= 0; --sz) {
+          const int groups = 1 << sz;
+          while (nk - qq >= groups) {
+            tma_load_3d(bs + (size_t)qq * kTcNT * 32, &tm_b.m[sz][l], 0, n_begin + c * kTcNT,
+                        k * (p.R16 / 16) + qq, &bfull[s]);
+            qq += groups;
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -332,63 +383,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mma_commit(&afull[s]);
       }
     }
-  } else {
+  } else if (warp < 2 + kExpTmemWarps) {
+    // ---------------- TMEM readers: acc * scale -> staging (row m, 16-byte chunk j at j ^ (m & 15))
     const int quad = warp & 3;
     const int m = quad * 32 + lane;
-    const int t = rb + m;
-    const bool row_valid = t < re;
-    const bool warp_full = rb + quad * 32 + 31 < re;
-    uint8_t* mybuf = ystage + (size_t)(warp - 2) * 2 * 4096;
-    int jj = 0;
-    for (int c = 0; c < nchunks; ++c) {
+    int hh = 0;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c & 1;
       if (!mbar_wait_or_fail(&afull[s], (c >> 1) & 1, &fail_sh)) {
         fail_sh = 1;
+        ok = false;
         break;
       }
       tc_fence_after();
-      const int nt = min(kTcNT, n_end - (n_begin + c * kTcNT));
-      const int col0 = p.off[l] + n_begin + c * kTcNT;
-      for (int j = 0; j < nt / 32; ++j, ++jj) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(s * kTcNT + 32 * j), v);
+      const int nhalf = min(kTcNT, n_end - (n_begin + c * kTcNT)) / kHalfCols;
+      for (int h = 0; h < nhalf; ++h, ++hh) {
+        const int sb = hh & 1;
+        if (hh >= 2 && !mbar_wait_or_fail(&sempty[sb], ((hh >> 1) - 1) & 1, &fail_sh)) {
+          fail_sh = 1;
+          ok = false;
+          break;
+        }
+        uint8_t* row = ystage + (size_t)sb * kHalfBytes + (size_t)m * (kHalfCols * 4);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] *= sc;
-        if (warp_full) {
-          uint8_t* buf = mybuf + (jj & 1) * 4096;
-          if (jj >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-          }
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<float4*>(buf + lane * 128 + ((ch ^ (lane & 7)) * 16)) =
-                make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_2d(&tm_y, col0 + 32 * j, rb + quad * 32, buf);
-            bulk_commit();
-          }
-        } else if (row_valid) {
-          float4* yp = reinterpret_cast<float4*>(p.y + (size_t)t * p.ldy + col0 + 32 * j);
+        for (int j = 0; j < 2; ++j) {
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(s * kTcNT + h * kHalfCols + 32 * j), v);
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
-            float4 a = yp[ch];
-            a.x += v[4 * ch];
-            a.y += v[4 * ch + 1];
-            a.z += v[4 * ch + 2];
-            a.w += v[4 * ch + 3];
-            yp[ch] = a;
+            const int cj = 8 * j + ch;
+            *reinterpret_cast<float4*>(row + ((cj ^ (m & 15)) * 16)) =
+                make_float4(v[4 * ch] * sc, v[4 * ch + 1] * sc, v[4 * ch + 2] * sc, v[4 * ch + 3] * sc);
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[sb]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&aempty[s]);
+      if (ok && lane == 0) mbar_arrive(&aempty[s]);
     }
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
+  } else {
+    // ---------------- y update: kRmwRowsPerWarp rows per warp; lanes 0-15 / 16-31 cover two rows of 64 columns
+    const int rw = warp - 2 - kExpTmemWarps;
+    const int chunk = lane & 15;
+    int total_h = 0;
+    for (int c = 0; c < nchunks; ++c) total_h += min(kTcNT, n_end - (n_begin + c * kTcNT)) / kHalfCols;
+    auto col_of = [&](int hidx) {  // first column of half chunk hidx (halves never straddle chunks)
+      return p.off[l] + n_begin + hidx * kHalfCols + 4 * chunk;
+    };
+    // y of the next two half chunks is in flight while the current one is added
+    float4 yv[kRmwRowsPerWarp / 2], yn[kRmwRowsPerWarp / 2], ynn[kRmwRowsPerWarp / 2];
+    auto load_half = [&](int hidx, float4 (&dst)[kRmwRowsPerWarp / 2]) {
+      const int col = col_of(hidx);
+#pragma unroll
+      for (int it = 0; it < kRmwRowsPerWarp / 2; ++it) {
+        const int row = 2 * kExpRmwWarps * it + 2 * rw + (lane >> 4);
+        const int t = rb + row;
+        if (t < re) dst[it] = *reinterpret_cast<const float4*>(p.y + (size_t)t * p.ldy + col);
+      }
+    };
+    if (total_h > 0) load_half(0, yv);
+    if (total_h > 1) load_half(1, yn);
+    for (int hh = 0; hh < total_h; ++hh) {
+      const int sb = hh & 1;
+      if (hh + 2 < total_h) load_half(hh + 2, ynn);
+      if (!mbar_wait_or_fail(&sfull[sb], (hh >> 1) & 1, &fail_sh)) {
+        fail_sh = 1;
+        break;
+      }
+      const uint8_t* st = ystage + (size_t)sb * kHalfBytes;
+      const int col = col_of(hh);
+#pragma unroll
+      for (int it = 0; it < kRmwRowsPerWarp / 2; ++it) {
+        const int row = 2 * kExpRmwWarps * it + 2 * rw + (lane >> 4);
+        const int t = rb + row;
+        if (t < re) {
+          const float4 d = *reinterpret_cast<const float4*>(st + (size_t)row * (kHalfCols * 4) +
+                                                            ((chunk ^ (row & 15)) * 16));
+          float4 a = yv[it];
+          a.x += d.x;
+          a.y += d.y;
+          a.z += d.z;
+          a.w += d.w;
+          *reinterpret_cast<float4*>(p.y + (size_t)t * p.ldy + col) = a;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[sb]);
+#pragma unroll
+      for (int it = 0; it < kRmwRowsPerWarp / 2; ++it) {
+        yv[it] = yn[it];
+        yn[it] = ynn[it];
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -399,20 +488,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
 }
 
-int tc_tile_bound(const lora_segments* seg) { return ceil_div(seg->T, kTcTile) + seg->S; }
+// Upper bound of tensor tiles for the last build: a sequence of q_len >= 64
+// gives ceil(q_len / 128) <= q_len / 64 tiles, so there are at most
+// min(T / 128 + S, T / 64) of them.
+int tc_tile_bound(const lora_segments* seg) {
+  const int a = ceil_div(seg->T, kTcTile) + seg->S, b = seg->T / LORA_TC_MIN_QLEN;
+  return a < b ? a : b;
+}
 
 }  // namespace
 
 int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
                      cudaStream_t st) {
-  const int grid = tc_tile_bound(seg);
+  const int grid = tc_tile_bound(seg) * kTcKSplit;
   if (grid <= 0) return LORA_OK;
-  CUtensorMap tm_x;
+  CUtensorMap tm_x128, tm_x32;
   {
     const uint64_t dims[2] = {(uint64_t)pool->d_in, (uint64_t)seg->T};
     const uint64_t strides[1] = {2ull * (uint64_t)ldx};
-    const uint32_t box[2] = {(uint32_t)kTcKBlock, (uint32_t)kXBoxRows};
-    if (!encode_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+    const uint32_t box128[2] = {(uint32_t)kTcKBlock, (uint32_t)kTcTile};
+    const uint32_t box32[2] = {(uint32_t)kTcKBlock, (uint32_t)kXBoxRows};
+    if (!encode_tmap(&tm_x128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&tm_x32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box32,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return LORA_ERR_CUDA;
   }
@@ -425,8 +523,10 @@ int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint
   p.L = pool->L;
   p.R16 = pool->R16;
   p.num_kb = pool->d_in / kTcKBlock;
+  p.u_split_stride = (size_t)pool->max_tokens * pool->L * pool->R16;
   p.stage_bytes = kXStageBytes + pool->L * pool->R16 * kTcKBlock * 2;
-  int stages = (200 * 1024) / p.stage_bytes;
+  // two CTAs per SM: each keeps its ring within ~100 KB of shared memory
+  int stages = (100 * 1024) / p.stage_bytes;
   if (stages > 6) stages = 6;
   if (stages < 2) stages = 2;
   p.stages = stages;
@@ -436,7 +536,7 @@ int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint
   const int smem = stages * p.stage_bytes + 1024;
   if (cudaFuncSetAttribute(tc_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return LORA_ERR_CUDA;
-  tc_shrink_kernel<<<grid, kTcThreads, smem, st>>>(tm_x, pool->tm_a, p);
+  tc_shrink_kernel<<<grid, kTcThreads, smem, st>>>(tm_x128, tm_x32, pool->tm_a, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
@@ -452,28 +552,21 @@ int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, 
   p.total_ng = p.ng_base[pool->L];
   const long long grid = (long long)tc_tile_bound(seg) * p.total_ng;
   if (grid <= 0) return LORA_OK;
-  CUtensorMap tm_y;
-  {
-    const uint64_t dims[2] = {(uint64_t)pool->D, (uint64_t)seg->T};
-    const uint64_t strides[1] = {4ull * (uint64_t)ldy};
-    const uint32_t box[2] = {32u, 32u};
-    if (!encode_tmap(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return LORA_ERR_CUDA;
-  }
   p.counts = seg->counts;
   p.work = seg->tc_work;
   p.rank_tab = pool->rank_tab;
   p.scale_tab = pool->scale_tab;
   p.u_tc = pool->u_tc;
+  p.u_split_stride = (size_t)pool->max_tokens * pool->L * pool->R16;
   p.y = y;
   p.ldy = ldy;
   p.status = seg->status;
   p.L = pool->L;
   p.R16 = pool->R16;
-  const int smem = 32768 + 4 * kTcTile * pool->R16 * 2 + 1024;  // staging + 2 B stages + U hi/lo
+  const int smem = 2 * kHalfBytes + 4 * kTcTile * pool->R16 * 2 + 1024;  // staging + 2 B stages + U hi/lo
   if (cudaFuncSetAttribute(tc_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return LORA_ERR_CUDA;
-  tc_expand_kernel<<<(unsigned)grid, kTcThreads, smem, st>>>(pool->tm_bk, tm_y, p);
+  tc_expand_kernel<<<(unsigned)grid, kExpThreads, smem, st>>>(pool->tm_bk, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }

@@ -168,6 +168,18 @@ def traffic_from_profile(kernel: str, workload: str):
         return None
 
 
+def truncate_workload(wl, n_seqs: int):
+    """The first n_seqs sequences of a workload (same adapters and factors)."""
+    n_seqs = min(n_seqs, wl.S)
+    T = int(wl.q_seq_lens[:n_seqs].sum())
+    out = W.Workload(wl.name + f"[:{n_seqs}]", wl.adapter_ids[:n_seqs].copy(), wl.q_seq_lens[:n_seqs].copy(),
+                     wl.num_slots)
+    for p in wl.projections:
+        out.projections.append(W.Projection(p.name, p.d_in, p.lane_d_out, p.rank, p.scale, p.A, p.B,
+                                            p.x[:T].copy(), p.y0[:T].copy(), p.max_rank))
+    return out
+
+
 # ------------------------------------------------------------ our arm
 
 def setup_device_workload(wl, dev):
@@ -359,6 +371,8 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     wl = W.make_workload(args.workload, seed=args.seed + rank)
+    if args.max_seqs:
+        wl = truncate_workload(wl, args.max_seqs)
     res, ctx = time_ours(wl, args.steps, args.warmup, dev, local)
     step_ms = max_over_ranks(res["step_ms"])
     units = algorithmic_units(wl)
@@ -512,6 +526,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--all-workloads", action="store_true", help="add a per_workload summary of the other configs")
+    ap.add_argument("--max-seqs", type=int, default=0,
+                    help="keep only the first N sequences of the workload (smaller case for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

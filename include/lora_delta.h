@@ -177,7 +177,7 @@ int lora_segments_destroy(lora_segments* seg);
  * Rows of slot 0, and lanes of rank 0, are neither read nor written.  Each
  * row's result depends only on its own x row, its adapter's factors and its
  * own sequence's length: sums run in fp32 in a fixed order (decode path:
- * shrink over d_in in fixed 2048-wide chunks reduced by a fixed tree, expand
+ * shrink over d_in in fixed 1024-wide chunks reduced by a fixed tree, expand
  * over the rank in ascending order, y = fma(scale, v, y); tensor path: tcgen05
  * bf16 MMAs with fp32 accumulation, the rank-space vector split into two bf16
  * halves for the expand, y = y + scale * v).
@@ -199,7 +199,7 @@ int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void
  * frozen after start-up.  No passage of the pages has a counterpart; this is a
  * property of the library, not of the method.
  *   - The rank-space intermediate (decode partial sums and tensor-path rank
- *     rows, (C + 1) * T * num_lanes * R16 floats with C = ceil(d_in / chunk))
+ *     rows, (C + 2) * T * num_lanes * R16 floats with C = ceil(d_in / 1024))
  *     lives in a fixed array compiled into the library, of
  *     LORA_NOALLOC_SCRATCH_BYTES; every GPU that loads the library holds it
  *     until the process exits.  A step that needs more returns LORA_ERR_SHAPE

@@ -60,7 +60,7 @@ def test_noalloc_rejects_a_step_beyond_its_scratch():
     import torch
     from adapter_gemv_lora_gb300 import lora_delta as LD
     # one 70000-row prefill chunk at rank 128 needs at least
-    # (1 decode chunk + 1) * 70000 * 128 * 4 bytes = 68 MiB > the 64 MiB scratch
+    # 3 partial rows x 70000 x 128 x 4 bytes = 103 MiB > the 64 MiB scratch
     T, d_in = 70000, 4096
     pool = LD.LoraPool(2, 128, d_in, [64], T)
     A = torch.zeros((128, d_in), dtype=torch.int16, device="cuda")

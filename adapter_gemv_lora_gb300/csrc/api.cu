@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -20,6 +21,26 @@ int sm_count(int device) {
     cache[device] = v;
   }
   return cache[device];
+}
+
+bool set_smem_limit(const void* kernel, int device, int bytes) {
+  struct Entry {
+    const void* kernel;
+    int device, bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : done)
+    if (e.kernel == kernel && e.device == device && e.bytes >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  for (Entry& e : done)
+    if (e.kernel == kernel && e.device == device) {
+      e.bytes = bytes;
+      return true;
+    }
+  done.push_back({kernel, device, bytes});
+  return true;
 }
 
 namespace {

@@ -402,8 +402,7 @@ int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uin
   const int grid = (int)(items < cap ? items : cap);
   if (grid <= 0) return LORA_OK;
   const int smem = (int)(kShRingBytes + kShRedBytes);
-  if (cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return LORA_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(dec_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   dec_shrink_kernel<<<grid, kShThreads, smem, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
@@ -418,8 +417,7 @@ int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y,
   const int grid = (int)(items < cap ? items : cap);
   if (grid <= 0) return LORA_OK;
   const int smem = (int)kExRingBytes;
-  if (cudaFuncSetAttribute(dec_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return LORA_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(dec_expand_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   dec_expand_kernel<<<grid, kExThreads, smem, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;

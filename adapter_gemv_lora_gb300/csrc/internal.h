@@ -87,6 +87,8 @@ namespace lora {
 
 extern std::atomic<uint64_t> g_launches;
 int sm_count(int device);
+// cudaFuncSetAttribute(max dynamic shared memory) once per (kernel, device, size).
+bool set_smem_limit(const void* kernel, int device, int bytes);
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* addr, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
 

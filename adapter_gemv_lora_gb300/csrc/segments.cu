@@ -71,16 +71,6 @@ __device__ int block_exclusive_scan(int v, int* sums, int& total) {
   return ex;
 }
 
-// Largest i in [0, n) with a[i] <= v (a non-decreasing, a[0] <= v).
-__device__ __forceinline__ int last_le(const int32_t* a, int n, int v) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (a[mid] <= v) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) {
   extern __shared__ int smem_dyn[];
   __shared__ int sums[33];
@@ -243,12 +233,14 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   }
   __syncthreads();
 
-  // ---- per-token slot and perm
-  for (int t = tid; t < T; t += kSegThreads) {
-    const int s = last_le(p.seq_start, S + 1, t);
-    const int id = p.ids[s];
-    p.slot[t] = id;
-    if (id != 0) p.perm[p.seq_pos[s] + (t - p.seq_start[s])] = t;
+  // ---- per-token slot and perm: one warp per sequence, coalesced writes
+  for (int s = warp; s < S; s += kSegThreads / 32) {
+    const int id = p.ids[s], st = p.seq_start[s], len = p.lens[s];
+    const int pos = id != 0 ? p.seq_pos[s] : 0;
+    for (int j = lane; j < len; j += 32) {
+      p.slot[st + j] = id;
+      if (id != 0) p.perm[pos + j] = st + j;
+    }
   }
 
   // ---- decode groups: slot k's class-0 run cut into runs of <= kDecGroup
@@ -309,11 +301,8 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
   p.dec_work = seg->dec_work;
   p.tc_work = seg->tc_work;
   const size_t sm = seg_smem_bytes(seg->N);
-  if (sm > 48 * 1024) {
-    if (cudaFuncSetAttribute(seg_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
-        cudaSuccess)
-      return LORA_ERR_CUDA;
-  }
+  if (sm > 48 * 1024 && !set_smem_limit(reinterpret_cast<const void*>(seg_build_kernel), seg->device, (int)sm))
+    return LORA_ERR_CUDA;
   seg_build_kernel<<<1, kSegThreads, sm, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;

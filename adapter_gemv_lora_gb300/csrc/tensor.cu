@@ -534,8 +534,7 @@ int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint
   while (cols < pool->L * pool->R16) cols <<= 1;
   p.tmem_cols = cols;
   const int smem = stages * p.stage_bytes + 1024;
-  if (cudaFuncSetAttribute(tc_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return LORA_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(tc_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   tc_shrink_kernel<<<grid, kTcThreads, smem, st>>>(tm_x128, tm_x32, pool->tm_a, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
@@ -564,8 +563,7 @@ int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, 
   p.L = pool->L;
   p.R16 = pool->R16;
   const int smem = 2 * kHalfBytes + 4 * kTcTile * pool->R16 * 2 + 1024;  // staging + 2 B stages + U hi/lo
-  if (cudaFuncSetAttribute(tc_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return LORA_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(tc_expand_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   tc_expand_kernel<<<(unsigned)grid, kExpThreads, smem, st>>>(pool->tm_bk, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;

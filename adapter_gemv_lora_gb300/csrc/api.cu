@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <mutex>
 #include <vector>
 
@@ -11,6 +12,16 @@
 namespace lora {
 
 std::atomic<uint64_t> g_launches{0};
+
+namespace {
+thread_local char t_last_error[256] = "";
+}
+
+int cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return LORA_OK;
+  snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  return LORA_ERR_CUDA;
+}
 
 int sm_count(int device) {
   static int cache[64] = {0};
@@ -33,7 +44,9 @@ bool set_smem_limit(const void* kernel, int device, int bytes) {
   std::lock_guard<std::mutex> lock(mu);
   for (const Entry& e : done)
     if (e.kernel == kernel && e.device == device && e.bytes >= bytes) return true;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  if (cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                  "cudaFuncSetAttribute(max dynamic shared memory)") != LORA_OK)
+    return false;
   for (Entry& e : done)
     if (e.kernel == kernel && e.device == device) {
       e.bytes = bytes;
@@ -159,5 +172,7 @@ const char* lora_status_string(int status) {
 }
 
 uint64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* lora_last_error_string(void) { return t_last_error; }
 
 }  // extern "C"

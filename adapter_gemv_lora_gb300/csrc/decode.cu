@@ -23,6 +23,7 @@
 //    chunk order.
 //  * expand: u is the in-order sum of the chunk partials; v[o] accumulates
 //    B[o][i] * u[i] for i = 0..r-1 in order with fma; y = fma(scale, v, y).
+//    Each compute thread owns 4 consecutive output columns of the group's rows.
 #include <cuda_runtime.h>
 
 #include "device.cuh"
@@ -38,14 +39,16 @@ constexpr int kShStages = 4;
 constexpr int kShMaxRb = 128 / kShRows;          // rank blocks for r <= 128
 constexpr size_t kShRingBytes = (size_t)kShStages * kShRows * kDecKChunk * 2;  // 64 KB
 constexpr size_t kShRedBytes = (size_t)kShWarps * kShMaxRb * 64 * 4;          // 16 KB
+constexpr size_t kShXBytes = (size_t)2 * kDecGroup * kDecKChunk * 2;           // 32 KB, x rows, two items
 static_assert(kShWarps * 256 == kDecKChunk, "one 8-element slice per lane covers a chunk");
 
-constexpr int kExWarps = 4;                      // expand compute warps (8 columns per thread)
+constexpr int kExWarps = 8;                      // expand compute warps (4 columns per thread)
 constexpr int kExThreads = (kExWarps + 1) * 32;
+constexpr int kExCols = 4;                       // output columns per compute thread
 constexpr int kExRows = 16;                      // rank rows per ring stage
 constexpr int kExStages = 3;
 constexpr size_t kExRingBytes = (size_t)kExStages * kExRows * kDecNChunk * 2;  // 96 KB
-static_assert(kExWarps * 32 * 8 == kDecNChunk, "8 columns per thread cover a chunk");
+static_assert(kExWarps * 32 * kExCols == kDecNChunk, "the compute threads cover a chunk");
 
 struct DecParams {
   const int32_t* counts;
@@ -83,7 +86,8 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* ring = reinterpret_cast<uint16_t*>(smem);         // [stage][row][kDecKChunk]
   float* red = reinterpret_cast<float*>(smem + kShRingBytes);  // [warp][rank block][64]
-  __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages];
+  uint16_t* xbuf = reinterpret_cast<uint16_t*>(smem + kShRingBytes + kShRedBytes);  // [2][row][kDecKChunk]
+  __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages], xfull[2], xempty[2];
   __shared__ int fail_sh;
 
   if (*p.status != 0) return;
@@ -96,15 +100,19 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kShWarps);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], kShWarps);
+    }
     fail_sh = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
   if (warp == kShWarps) {
-    // ---------------- producer: stream the slot's A rows of this chunk
+    // ---------------- producer: the group's x rows of this chunk, then the slot's A rows
     if (lane == 0) {
-      uint32_t fill = 0;
+      uint32_t fill = 0, xj = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int w = item / per_group, rem = item - w * per_group;
@@ -113,6 +121,20 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
         const int r = p.rank_tab[k * p.L + l];
         if (r <= 0) continue;
         const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
+        {
+          const int4 g = p.work[w];
+          const int nrows = g.z - g.y, xs = xj & 1;
+          if (xj >= 2 && !mbar_wait_or_fail(&xempty[xs], ((xj >> 1) - 1) & 1, &fail_sh)) {
+            ok = false;
+            fail_sh = 1;
+            break;
+          }
+          mbar_expect_tx(&xfull[xs], (uint32_t)(nrows * klen * 2));
+          for (int gg = 0; gg < nrows; ++gg)
+            bulk_load(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk,
+                      p.x + (size_t)p.perm[g.y + gg] * p.ldx + k0, (uint32_t)(klen * 2), &xfull[xs]);
+          ++xj;
+        }
         const uint16_t* Ab = p.A[l] + (size_t)k * p.R16 * p.d_in + k0;
         for (int rb = 0; rb < r; rb += kShRows, ++fill) {
           const int s = fill % kShStages;
@@ -131,7 +153,7 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
     }
   } else {
     // ---------------- compute warps
-    uint32_t use = 0;
+    uint32_t use = 0, xj = 0;
     bool ok = true;
     const int kk = warp * 256 + lane * 8;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -143,17 +165,24 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
       if (r <= 0) continue;
       const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
       const bool has_k = kk < klen;
+      const int xs = xj & 1;
+      if (ok && !mbar_wait_or_fail(&xfull[xs], (xj >> 1) & 1, &fail_sh)) {
+        ok = false;
+        fail_sh = 1;
+      }
       float xv[kDecGroup][8];
 #pragma unroll
       for (int gg = 0; gg < kDecGroup; ++gg) {
-        if (gg < nrows && has_k) {
-          const int t = p.perm[p0 + gg];
-          unpack8(ldg_nc_v4(p.x + (size_t)t * p.ldx + k0 + kk), xv[gg]);
+        if (ok && gg < nrows && has_k) {
+          unpack8(*reinterpret_cast<const uint4*>(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk + kk), xv[gg]);
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e) xv[gg][e] = 0.f;
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xempty[xs]);
+      ++xj;
       const int nrb = (r + kShRows - 1) / kShRows;
       for (int rb = 0; rb < nrb; ++rb, ++use) {
         const int s = use % kShStages;
@@ -207,7 +236,7 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
   if (tid == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kExThreads) dec_expand_kernel(DecParams p) {
+__global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* ring = reinterpret_cast<uint16_t*>(smem);  // [stage][row][kDecNChunk]
   __shared__ __align__(16) float us[128][kDecGroup];   // [rank][row]
@@ -262,7 +291,7 @@ __global__ void __launch_bounds__(kExThreads) dec_expand_kernel(DecParams p) {
       }
     }
   } else {
-    // ---------------- compute warps: 8 output columns per thread
+    // ---------------- compute warps: kExCols output columns per thread
     uint32_t use = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -287,25 +316,18 @@ __global__ void __launch_bounds__(kExThreads) dec_expand_kernel(DecParams p) {
         us[i][gg] = s;
       }
       named_bar_sync(1, kExWarps * 32);
-      const int o = n0 + 8 * tid;
+      const int o = n0 + kExCols * tid;
       const bool has = o < dout;
-      float4 yv[kDecGroup][2];
-      float* yrow[kDecGroup];
+      float4 yv[kDecGroup];
+      float* const ycol = p.y + p.off[l] + o;
 #pragma unroll
-      for (int gg = 0; gg < kDecGroup; ++gg) {
-        yrow[gg] = nullptr;
-        if (has && gg < nrows) {
-          const int t = p.perm[p0 + gg];
-          yrow[gg] = p.y + (size_t)t * p.ldy + p.off[l] + o;
-          yv[gg][0] = *reinterpret_cast<const float4*>(yrow[gg]);
-          yv[gg][1] = *reinterpret_cast<const float4*>(yrow[gg] + 4);
-        }
-      }
-      float acc[kDecGroup][8];
+      for (int gg = 0; gg < kDecGroup; ++gg)
+        if (has && gg < nrows) yv[gg] = *reinterpret_cast<const float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy);
+      float acc[kDecGroup][kExCols];
 #pragma unroll
       for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[gg][e] = 0.f;
+        for (int e = 0; e < kExCols; ++e) acc[gg][e] = 0.f;
       const int nrb = (r + kExRows - 1) / kExRows;
       for (int rb = 0; rb < nrb; ++rb, ++use) {
         const int s = use % kExStages;
@@ -314,20 +336,20 @@ __global__ void __launch_bounds__(kExThreads) dec_expand_kernel(DecParams p) {
           fail_sh = 1;
         }
         if (ok && has) {
-          const uint16_t* st = ring + (size_t)s * kExRows * kDecNChunk + 8 * tid;
+          const uint16_t* st = ring + (size_t)s * kExRows * kDecNChunk + kExCols * tid;
 #pragma unroll 4
           for (int i = 0; i < kExRows; ++i) {
             const int ri = rb * kExRows + i;
             if (ri < r) {
-              float bv[8];
-              unpack8(*reinterpret_cast<const uint4*>(st + (size_t)i * kDecNChunk), bv);
+              const uint2 q2 = *reinterpret_cast<const uint2*>(st + (size_t)i * kDecNChunk);
+              const float bv[kExCols] = {bf16lo(q2.x), bf16hi(q2.x), bf16lo(q2.y), bf16hi(q2.y)};
               const float4 u0 = *reinterpret_cast<const float4*>(&us[ri][0]);
               const float4 u1 = *reinterpret_cast<const float4*>(&us[ri][4]);
               const float ug[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
               for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[gg][e] = fmaf(bv[e], ug[gg], acc[gg][e]);
+                for (int e = 0; e < kExCols; ++e) acc[gg][e] = fmaf(bv[e], ug[gg], acc[gg][e]);
             }
           }
         }
@@ -339,17 +361,12 @@ __global__ void __launch_bounds__(kExThreads) dec_expand_kernel(DecParams p) {
 #pragma unroll
       for (int gg = 0; gg < kDecGroup; ++gg) {
         if (gg < nrows) {
-          float4 a = yv[gg][0], b = yv[gg][1];
+          float4 a = yv[gg];
           a.x = fmaf(sc, acc[gg][0], a.x);
           a.y = fmaf(sc, acc[gg][1], a.y);
           a.z = fmaf(sc, acc[gg][2], a.z);
           a.w = fmaf(sc, acc[gg][3], a.w);
-          b.x = fmaf(sc, acc[gg][4], b.x);
-          b.y = fmaf(sc, acc[gg][5], b.y);
-          b.z = fmaf(sc, acc[gg][6], b.z);
-          b.w = fmaf(sc, acc[gg][7], b.w);
-          *reinterpret_cast<float4*>(yrow[gg]) = a;
-          *reinterpret_cast<float4*>(yrow[gg] + 4) = b;
+          *reinterpret_cast<float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy) = a;
         }
       }
     }
@@ -401,11 +418,11 @@ int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uin
   const long long cap = 2LL * sm_count(pool->device);
   const int grid = (int)(items < cap ? items : cap);
   if (grid <= 0) return LORA_OK;
-  const int smem = (int)(kShRingBytes + kShRedBytes);
+  const int smem = (int)(kShRingBytes + kShRedBytes + kShXBytes);
   if (!set_smem_limit(reinterpret_cast<const void*>(dec_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   dec_shrink_kernel<<<grid, kShThreads, smem, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return cuda_status(cudaGetLastError(), "dec_shrink_kernel launch");
 }
 
 int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {
@@ -420,7 +437,7 @@ int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y,
   if (!set_smem_limit(reinterpret_cast<const void*>(dec_expand_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   dec_expand_kernel<<<grid, kExThreads, smem, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return cuda_status(cudaGetLastError(), "dec_expand_kernel launch");
 }
 
 }  // namespace lora

@@ -87,6 +87,9 @@ namespace lora {
 
 extern std::atomic<uint64_t> g_launches;
 int sm_count(int device);
+// Record a failed CUDA call (its text is kept per thread for lora_last_error_string)
+// and map it to LORA_ERR_CUDA; cudaSuccess maps to LORA_OK.
+int cuda_status(cudaError_t e, const char* where);
 // cudaFuncSetAttribute(max dynamic shared memory) once per (kernel, device, size).
 bool set_smem_limit(const void* kernel, int device, int bytes);
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* addr, const uint64_t* dims,

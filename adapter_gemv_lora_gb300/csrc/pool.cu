@@ -105,7 +105,7 @@ int launch_repack(lora_pool* pool, int slot, int lane, int rank, float scale, co
                                          pool->rank_tab + slot * pool->L + lane,
                                          pool->scale_tab + slot * pool->L + lane, scale);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return cuda_status(cudaGetLastError(), "repack_kernel launch");
 }
 
 }  // namespace lora

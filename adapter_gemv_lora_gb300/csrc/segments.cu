@@ -305,7 +305,7 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
     return LORA_ERR_CUDA;
   seg_build_kernel<<<1, kSegThreads, sm, st>>>(p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return cuda_status(cudaGetLastError(), "seg_build_kernel launch");
 }
 
 }  // namespace lora

@@ -284,7 +284,13 @@ __global__ void __launch_bounds__(kExpThreads, 1)
     tmem_alloc(&tmem_base_sh, 2 * kTcNT);
     tmem_relinquish();
   }
-  // U rows -> bf16 hi / lo halves in the K-major core-matrix layout.
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  // U rows -> bf16 hi / lo halves in the K-major core-matrix layout (the B
+  // tiles are already on their way meanwhile; the MMA warp waits on a named
+  // barrier for these halves only).
   if (warp >= 2 && warp < 2 + kExpTmemWarps) {
     const int m = (warp & 3) * 32 + lane;
     const int t = rb + m;
@@ -321,11 +327,8 @@ __global__ void __launch_bounds__(kExpThreads, 1)
       *reinterpret_cast<uint4*>(ulo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     fence_proxy_async_smem();
+    named_bar_sync(1, 32 + kExpTmemWarps * 32);
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -352,6 +355,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
       }
     }
   } else if (warp == 1) {
+    named_bar_sync(1, 32 + kExpTmemWarps * 32);  // U halves written
     if (lane == 0) {
       const uint32_t uh = smem_u32(uhi), ul = smem_u32(ulo);
       for (int c = 0; c < nchunks; ++c) {
@@ -537,7 +541,7 @@ int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint
   if (!set_smem_limit(reinterpret_cast<const void*>(tc_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   tc_shrink_kernel<<<grid, kTcThreads, smem, st>>>(tm_x128, tm_x32, pool->tm_a, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return cuda_status(cudaGetLastError(), "tc_shrink_kernel launch");
 }
 
 int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {
@@ -566,7 +570,7 @@ int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, 
   if (!set_smem_limit(reinterpret_cast<const void*>(tc_expand_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   tc_expand_kernel<<<(unsigned)grid, kExpThreads, smem, st>>>(pool->tm_bk, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  return cuda_status(cudaGetLastError(), "tc_expand_kernel launch");
 }
 
 }  // namespace lora

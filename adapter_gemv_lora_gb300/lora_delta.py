@@ -63,6 +63,7 @@ def load_library(path: str = LIB_PATH):
         "lora_apply_shrink_expand_noalloc": (I, [P, P, P, P, I64, I64, P]),
         "lora_status_string": (ctypes.c_char_p, [I]),
         "lora_launch_count": (ctypes.c_uint64, []),
+        "lora_last_error_string": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -74,7 +75,8 @@ def load_library(path: str = LIB_PATH):
 
 def _check(st: int, what: str):
     if st != LORA_OK:
-        raise LoraError(st, what)
+        detail = lora_last_error_string() if st == LORA_ERR_CUDA else ""
+        raise LoraError(st, f"{what} [{detail}]" if detail else what)
 
 
 def _arr(vals, ctype):
@@ -85,6 +87,10 @@ def _arr(vals, ctype):
 
 def lora_status_string(status: int) -> str:
     return load_library().lora_status_string(int(status)).decode()
+
+
+def lora_last_error_string() -> str:
+    return load_library().lora_last_error_string().decode()
 
 
 def lora_launch_count() -> int:

@@ -222,6 +222,10 @@ int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lora_segments*
 /* Text of a status code. */
 const char* lora_status_string(int status);
 
+/* Text of the last failed CUDA call made by this library on the calling
+ * thread (empty if none): what a LORA_ERR_CUDA came from. */
+const char* lora_last_error_string(void);
+
 /* Kernels this library has launched in this process (all entry points). */
 uint64_t lora_launch_count(void);
 

@@ -74,8 +74,7 @@ __device__ int block_exclusive_scan(int v, int* sums, int& total) {
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) {
   extern __shared__ int smem_dyn[];
   __shared__ int sums[33];
-  __shared__ int bad_len, bad_id;
-  __shared__ unsigned long long total_len;
+  __shared__ long long warp_len[kSegThreads / 32];
 
   const int N = p.N, S = p.S, T = p.T;
   int* cnt_tok = smem_dyn;            // [2N]  rows per (class, slot)
@@ -88,27 +87,28 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // ---- validation
-  if (tid == 0) {
-    bad_len = 0;
-    bad_id = 0;
-    total_len = 0;
-  }
+  // ---- validation (block reductions, no contended atomics)
   for (int i = tid; i < 2 * N; i += kSegThreads) cnt_tok[i] = 0;
   for (int i = tid; i < N; i += kSegThreads) cnt_tile[i] = 0;
-  __syncthreads();
-  unsigned long long my_sum = 0;
+  long long my_sum = 0;
+  int my_bad_len = 0, my_bad_id = 0;
   for (int s = tid; s < S; s += kSegThreads) {
     const int len = p.lens[s], id = p.ids[s];
-    if (len < 0) bad_len = 1;
-    if (id < 0 || id >= N) bad_id = 1;
-    my_sum += (unsigned long long)(long long)len;
+    my_bad_len |= len < 0;
+    my_bad_id |= (id < 0 || id >= N);
+    my_sum += len;
   }
-  if (my_sum) atomicAdd(&total_len, my_sum);
-  __syncthreads();
-  if (bad_len || (long long)total_len != (long long)T || bad_id) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) my_sum += __shfl_xor_sync(0xffffffffu, my_sum, o);
+  if (lane == 0) warp_len[warp] = my_sum;
+  const int bad_len = __syncthreads_or(my_bad_len);
+  const int bad_id = __syncthreads_or(my_bad_id);
+  long long total_len = 0;
+#pragma unroll 8
+  for (int w = 0; w < kSegThreads / 32; ++w) total_len += warp_len[w];
+  if (bad_len || total_len != (long long)T || bad_id) {
     if (tid < 4) p.counts[tid] = 0;
-    if (tid == 0) *p.status = (bad_len || (long long)total_len != (long long)T) ? LORA_ERR_META : LORA_ERR_SLOT;
+    if (tid == 0) *p.status = (bad_len || total_len != (long long)T) ? LORA_ERR_META : LORA_ERR_SLOT;
     return;
   }
 
@@ -124,13 +124,31 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   }
   if (tid == 0) p.seq_start[S] = T;
 
-  // ---- histogram of rows per (class, slot) and class-1 tiles per slot
-  for (int s = tid; s < S; s += kSegThreads) {
-    const int len = p.lens[s], id = p.ids[s];
-    if (id != 0 && len > 0) {
-      const int cls = len >= LORA_TC_MIN_QLEN ? 1 : 0;
-      atomicAdd(&cnt_tok[cls * N + id], len);
-      if (cls) atomicAdd(&cnt_tile[id], (len + kTcTile - 1) / kTcTile);
+  // ---- histogram of rows per (class, slot) and class-1 tiles per slot; lanes
+  // with the same key add up first, so each warp issues one atomic per key
+  for (int b = 0; b < S; b += kSegThreads) {
+    const int s = b + tid;
+    int key = -1, len = 0, nt = 0, id = 0;
+    if (s < S) {
+      len = p.lens[s];
+      id = p.ids[s];
+      if (id != 0 && len > 0) {
+        const int cls = len >= LORA_TC_MIN_QLEN ? 1 : 0;
+        key = cls * N + id;
+        nt = cls ? (len + kTcTile - 1) / kTcTile : 0;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(peers) - 1;
+    int gl = 0, gt = 0;
+    for (unsigned m = peers; m; m &= m - 1) {
+      const int j = __ffs(m) - 1;
+      gl += __shfl_sync(peers, len, j);
+      gt += __shfl_sync(peers, nt, j);
+    }
+    if (key >= 0 && lane == leader) {
+      atomicAdd(&cnt_tok[key], gl);
+      if (gt) atomicAdd(&cnt_tile[id], gt);
     }
   }
   __syncthreads();

@@ -99,6 +99,31 @@ using namespace lora;
 
 namespace {
 
+// A non-blocking side stream and two events per device, created on first use
+// (no device memory is allocated).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+
+SideStream* side_stream() {
+  static SideStream sides[64];
+  static bool ready[64] = {};
+  static std::mutex init_mu;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(init_mu);
+  SideStream& s = sides[dev];
+  if (!ready[dev]) {
+    if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    ready[dev] = true;
+  }
+  return &s;
+}
+
 bool any_loaded(const lora_pool* pool) {
   for (int v : pool->h_rank)
     if (v > 0) return true;
@@ -141,11 +166,33 @@ int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, co
   if (chk != LORA_OK) return chk;
   if (seg->T == 0 || !any_loaded(pool)) return LORA_OK;  // a layer no adapter edits launches nothing
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  for (int stage = 1; stage <= 4; ++stage) {
-    const int r = apply_stage(pool, seg, x, y, ldx, ldy, stage, st);
-    if (r != LORA_OK) return r;
+  SideStream* side = side_stream();
+  if (!side) {
+    for (int stage = 1; stage <= 4; ++stage) {
+      const int r = apply_stage(pool, seg, x, y, ldx, ldy, stage, st);
+      if (r != LORA_OK) return r;
+    }
+    return LORA_OK;
   }
-  return LORA_OK;
+  // The decode-path kernels (latency-bound, few bytes) run on a side stream
+  // while the tensor-path kernels (bandwidth-bound) run on the caller's
+  // stream; the two touch disjoint rows of y and share only the metadata the
+  // segment builder wrote before this call.  Fork and join are events, so the
+  // call stays ordered on the caller's stream and can be stream-captured.
+  std::lock_guard<std::mutex> lock(side->mu);
+  int r = cuda_status(cudaEventRecord(side->fork, st), "cudaEventRecord(fork)");
+  if (r == LORA_OK) r = cuda_status(cudaStreamWaitEvent(side->stream, side->fork, 0), "cudaStreamWaitEvent(fork)");
+  if (r != LORA_OK) return r;
+  int rd = apply_stage(pool, seg, x, y, ldx, ldy, 1, side->stream);
+  if (rd == LORA_OK) rd = apply_stage(pool, seg, x, y, ldx, ldy, 2, side->stream);
+  int rt = apply_stage(pool, seg, x, y, ldx, ldy, 3, st);
+  if (rt == LORA_OK) rt = apply_stage(pool, seg, x, y, ldx, ldy, 4, st);
+  // join even after a failed launch, so the caller's stream never runs ahead
+  r = cuda_status(cudaEventRecord(side->join, side->stream), "cudaEventRecord(join)");
+  if (r == LORA_OK) r = cuda_status(cudaStreamWaitEvent(st, side->join, 0), "cudaStreamWaitEvent(join)");
+  if (rd != LORA_OK) return rd;
+  if (rt != LORA_OK) return rt;
+  return r;
 }
 
 int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y, int64_t ldx,

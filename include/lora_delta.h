@@ -181,6 +181,10 @@ int lora_segments_destroy(lora_segments* seg);
  * over the rank in ascending order, y = fma(scale, v, y); tensor path: tcgen05
  * bf16 MMAs with fp32 accumulation, the rank-space vector split into two bf16
  * halves for the expand, y = y + scale * v).
+ * The decode-path kernels run on a side stream the library creates per device
+ * (forked from and joined back to `stream` with events), concurrently with the
+ * tensor-path kernels on `stream`; the call stays ordered on `stream` and can
+ * be stream-captured.
  * If the step has no rows, or the pool has no loaded lane, nothing is
  * launched.  Errors: LORA_ERR_ARG, LORA_ERR_SHAPE, LORA_ERR_CUDA; device
  * timeouts set LORA_ERR_TIMEOUT in the segments' status word. */

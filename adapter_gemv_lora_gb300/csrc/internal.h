@@ -38,6 +38,9 @@ struct TmapLanes {
 // loaded with one TMA copy per set bit of r16 / 16.  Sizes above the pool's
 // R16 are left zeroed and never used.
 constexpr int kTmapSizes = 4;
+// Tensor tiles a build can make: a sequence of q_len >= 64 gives at most
+// q_len / 64 tiles, so T rows give at most T / 64.
+inline int tc_tile_cap(int max_tokens) { return max_tokens / LORA_TC_MIN_QLEN + 1; }
 struct TmapSized {
   CUtensorMap m[kTmapSizes][LORA_MAX_LANES];
 };
@@ -58,7 +61,10 @@ struct lora_pool {
   uint16_t* Bk[LORA_MAX_LANES] = {};  // per lane [N][R16/16][d_out][16] (tensor expand: K-major
                                       // groups of 16 rank columns, each group contiguous)
   float* u_dec = nullptr;           // [C_dec][max_tokens][L][R16] split-K partial sums
-  float* u_tc = nullptr;            // [kTcKSplit][max_tokens][L][R16] partial sums over K ranges
+  float* u_tc = nullptr;            // [kTcKSplit][tc_tile_cap][L][R16/4][128] float4 partial sums over K ranges
+  uint16_t* u_fmt = nullptr;        // [tc_tile_cap][L][2][128*R16] per tensor tile: U as bf16 hi then lo,
+                                    // K-major core-matrix layout of the tile's own rank, ready for the expand
+  int32_t* tile_cnt = nullptr;      // [tc_tile_cap] K-range CTAs of a tile that finished (0 between calls)
   std::vector<int> h_rank;          // host mirror of rank_tab
   lora::TmapSized tm_a;             // A, 3-D {d_in, R16, N}, box {64, 16<<s, 1}, 128-byte swizzle
   lora::TmapSized tm_bk;            // Bk, 3-D {16, d_out, R16/16*N}, box {16, 128, 1<<s}, 32-byte swizzle

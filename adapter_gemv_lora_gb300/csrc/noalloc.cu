@@ -25,6 +25,11 @@
 namespace {
 
 constexpr size_t kScratchFloats = (size_t)LORA_NOALLOC_SCRATCH_BYTES / sizeof(float);
+// Per-tile arrival counters of the tensor shrink sit at the start of the
+// array, where they keep their between-calls value of zero (the array is
+// zero when the library loads, and each call leaves the counts it used at
+// zero).
+constexpr size_t kCounterWords = 16384;
 
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
@@ -58,12 +63,17 @@ extern "C" int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lor
   for (int v : pool->h_rank) loaded |= v > 0;
   if (T == 0 || !loaded) return LORA_OK;  // nothing to do: nothing is launched
 
-  // Rank-space scratch this step needs: decode partials [C][T][L][R16] plus
-  // tensor-path partial rows [kTcKSplit][T][L][R16], fp32.
+  // Rank-space scratch this step needs after the counters: decode partials
+  // [C][T][L][R16] and tensor-path partial tiles [kTcKSplit][tiles][L][R16*128]
+  // (fp32), then the tensor tiles' U blocks [tiles][L][2][128*R16] (bf16).
+  // The kernels size the tile regions from the view's max_tokens, set to T.
   const size_t per_row = (size_t)pool->L * pool->R16;
+  const size_t tiles = (size_t)lora::tc_tile_cap(T);
   const size_t dec_floats = (size_t)pool->C_dec * T * per_row;
-  const size_t need = dec_floats + (size_t)lora::kTcKSplit * T * per_row;
-  if (need > kScratchFloats) return LORA_ERR_SHAPE;
+  const size_t tc_floats = (size_t)lora::kTcKSplit * tiles * per_row * lora::kTcTile;
+  const size_t fmt_floats = tiles * per_row * lora::kTcTile;  // 2 bf16 halves = 1 float per element
+  const size_t need = kCounterWords + dec_floats + tc_floats + fmt_floats;
+  if (tiles > kCounterWords || need > kScratchFloats) return LORA_ERR_SHAPE;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
@@ -97,8 +107,10 @@ extern "C" int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lor
   view.scale_tab = pool->scale_tab;
   view.tm_a = pool->tm_a;
   view.tm_bk = pool->tm_bk;
-  view.u_dec = scratch;
-  view.u_tc = scratch + dec_floats;
+  view.tile_cnt = reinterpret_cast<int32_t*>(scratch);
+  view.u_dec = scratch + kCounterWords;
+  view.u_tc = view.u_dec + dec_floats;
+  view.u_fmt = reinterpret_cast<uint16_t*>(view.u_tc + tc_floats);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);

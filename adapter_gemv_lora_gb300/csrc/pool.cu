@@ -16,8 +16,14 @@
 //                                       one TMA box loads several whole groups
 //                                       for the tensor-core expand
 //   u_dec     f32   [C][max_tokens][L][R16]  decode split-K partial sums
-//   u_tc      f32   [2][max_tokens][L][R16]  tensor-path rank-space rows, one
-//                                            partial sum per half of d_in
+//   u_tc      f32   [2][tiles][L][R16*128]   tensor-path partial sums, one per
+//                                            half of d_in, per tile as
+//                                            [column quad][row] float4
+//   u_fmt     bf16  [tiles][L][2][128*R16]   per tensor tile the summed U as
+//                                            bf16 hi and lo halves, in the
+//                                            layout the expand's MMA reads
+//   tile_cnt  int32 [tiles]                  per tile, K-range CTAs done
+// (tiles = max_tokens / 64 + 1, the most a build can make)
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -55,7 +61,8 @@ __global__ void repack_kernel(const uint16_t* __restrict__ A, const uint16_t* __
 }
 
 struct PoolLayout {
-  size_t rank_tab, scale_tab, A[LORA_MAX_LANES], Bt[LORA_MAX_LANES], Bk[LORA_MAX_LANES], u_dec, u_tc, total;
+  size_t rank_tab, scale_tab, A[LORA_MAX_LANES], Bt[LORA_MAX_LANES], Bk[LORA_MAX_LANES], u_dec, u_tc, u_fmt, tile_cnt,
+      total;
   int R16, C_dec;
 };
 
@@ -85,7 +92,9 @@ bool pool_layout(int N, int R, int d_in, int L, const int* d_out, int max_tokens
     P->Bk[l] = o; o = align1k(o + 2 * (size_t)N * d_out[l] * R16);
   }
   P->u_dec = o; o = align1k(o + 4 * (size_t)P->C_dec * max_tokens * L * R16);
-  P->u_tc = o; o = align1k(o + 4 * (size_t)kTcKSplit * max_tokens * L * R16);
+  P->u_tc = o; o = align1k(o + 4 * (size_t)kTcKSplit * tc_tile_cap(max_tokens) * L * R16 * kTcTile);
+  P->u_fmt = o; o = align1k(o + 2 * (size_t)tc_tile_cap(max_tokens) * L * 2 * kTcTile * R16);
+  P->tile_cnt = o; o = align1k(o + 4 * (size_t)tc_tile_cap(max_tokens));
   P->total = o;
   return true;
 }
@@ -154,6 +163,8 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   p->scale_tab = reinterpret_cast<float*>(b + P.scale_tab);
   p->u_dec = reinterpret_cast<float*>(b + P.u_dec);
   p->u_tc = reinterpret_cast<float*>(b + P.u_tc);
+  p->u_fmt = reinterpret_cast<uint16_t*>(b + P.u_fmt);
+  p->tile_cnt = reinterpret_cast<int32_t*>(b + P.tile_cnt);
   p->h_rank.assign((size_t)num_slots * num_lanes, 0);
   std::memset(&p->tm_a, 0, sizeof(p->tm_a));
   std::memset(&p->tm_bk, 0, sizeof(p->tm_bk));

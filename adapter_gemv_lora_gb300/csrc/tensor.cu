@@ -35,14 +35,19 @@ namespace {
 constexpr int kXBoxRows = 32;                          // TMA box rows of X
 constexpr int kXStageBytes = kTcTile * kTcKBlock * 2;  // 16 KB
 constexpr int kMaxStages = 8;
+// X blocks are pulled into L2 this many k-blocks ahead of their load, which
+// keeps more HBM reads in flight than the shared-memory ring alone holds.
+constexpr int kXPrefetch = 0;
 
 struct TcShrinkParams {
   const int32_t* counts;
   const int4* work;
   const int32_t* rank_tab;
   float* u_tc;
+  uint16_t* u_fmt;
+  int32_t* tile_cnt;
   int32_t* status;
-  int L, R16, num_kb, stages, stage_bytes, tmem_cols;
+  int L, R16, num_kb, ring_bytes, tmem_cols, tiles_cap;
   size_t u_split_stride;  // floats between the K-range partials of u_tc
 };
 
@@ -51,8 +56,7 @@ struct TcExpandParams {
   const int4* work;
   const int32_t* rank_tab;
   const float* scale_tab;
-  const float* u_tc;
-  size_t u_split_stride;
+  const uint16_t* u_fmt;
   float* y;
   int32_t* status;
   int64_t ldy;
@@ -72,11 +76,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t done_bar;
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int fail_sh;
+  __shared__ int fail_sh, last_sh;
 
-  if (*p.status != 0) return;
+  // A timeout is the only status a kernel of this step can raise while this
+  // one runs; every other error is set before the launch and seen by all CTAs
+  // alike, which keeps the per-tile arrival counts consistent.
+  {
+    const int st0 = *p.status;
+    if (st0 != 0 && st0 != LORA_ERR_TIMEOUT) return;
+  }
   // CTA = (tile, K range): the k-blocks of d_in are cut into kTcKSplit fixed
-  // ranges; each CTA sums one range and the expand adds the partials in order.
+  // ranges; each CTA sums one range, and the last CTA of the tile to finish
+  // adds the partials in K order and writes U for the expand.
   const int tile = blockIdx.x / kTcKSplit;
   const int ksplit = blockIdx.x - tile * kTcKSplit;
   if (tile >= p.counts[3]) return;
@@ -84,25 +95,32 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int nkb = kb_hi - kb_lo;
   const int4 wk = p.work[tile];
   const int k = wk.x, rb = wk.y, re = wk.z;
-  int r16[LORA_MAX_LANES];
-  bool any = false;
+  int r16[LORA_MAX_LANES], a_off[LORA_MAX_LANES];
+  int r16_sum = 0;
 #pragma unroll
   for (int l = 0; l < LORA_MAX_LANES; ++l) {
     const int r = l < p.L ? p.rank_tab[k * p.L + l] : 0;
     r16[l] = r > 0 ? (r + 15) & ~15 : 0;
-    any |= r > 0;
+    a_off[l] = r16_sum;
+    r16_sum += r16[l];
   }
-  if (!any) return;
+  if (r16_sum == 0) return;
+  // Each stage holds one X block and the A blocks of the loaded lanes at
+  // their own ranks, so low-rank tiles keep more stages in flight.
+  const int stage_bytes = kXStageBytes + r16_sum * kTcKBlock * 2;
+  int stages = p.ring_bytes / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
 
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&done_bar, 1);
     fail_sh = 0;
+    last_sh = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -118,22 +136,32 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // sequence takes 32-row boxes up to its end.
   const bool full_tile = (re - rb) == kTcTile;
   const int nbox = (re - rb + kXBoxRows - 1) / kXBoxRows;
-  uint32_t tx_bytes = (uint32_t)(full_tile ? kTcTile : nbox * kXBoxRows) * kTcKBlock * 2;
-#pragma unroll
-  for (int l = 0; l < LORA_MAX_LANES; ++l) tx_bytes += (uint32_t)r16[l] * kTcKBlock * 2;
+  const uint32_t tx_bytes =
+      (uint32_t)(full_tile ? kTcTile : nbox * kXBoxRows) * kTcKBlock * 2 + (uint32_t)r16_sum * kTcKBlock * 2;
 
   if (warp == 0) {
     if (lane == 0) {
+      auto prefetch_x = [&](int kj) {
+        const int c0 = (kb_lo + kj) * kTcKBlock;
+        if (full_tile) {
+          tma_prefetch_2d(&tm_x128, c0, rb);
+        } else {
+          for (int b = 0; b < nbox; ++b) tma_prefetch_2d(&tm_x32, c0, rb + kXBoxRows * b);
+        }
+      };
+      if (kXPrefetch > 0)
+        for (int kj = stages; kj < kXPrefetch && kj < nkb; ++kj) prefetch_x(kj);
       for (int kj = 0; kj < nkb; ++kj) {
         const int kb = kb_lo + kj;
-        const int s = kj % p.stages;
-        if (kj >= p.stages) {
-          if (!mbar_wait_or_fail(&empty_bar[s], ((kj / p.stages) - 1) & 1, &fail_sh)) {
+        const int s = kj % stages;
+        if (kXPrefetch > 0 && kj + kXPrefetch < nkb) prefetch_x(kj + kXPrefetch);
+        if (kj >= stages) {
+          if (!mbar_wait_or_fail(&empty_bar[s], ((kj / stages) - 1) & 1, &fail_sh)) {
             fail_sh = 1;
             break;
           }
         }
-        uint8_t* xs = smem + (size_t)s * p.stage_bytes;
+        uint8_t* xs = smem + (size_t)s * stage_bytes;
         uint8_t* as = xs + kXStageBytes;
         mbar_expect_tx(&full_bar[s], tx_bytes);
         if (full_tile) {
@@ -149,7 +177,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           for (int sz = kTmapSizes - 1; sz >= 0; --sz) {
             const int rows = 16 << sz;
             while (r16[l] - row >= rows) {
-              tma_load_3d(as + (size_t)(l * p.R16 + row) * kTcKBlock * 2, &tm_a.m[sz][l], kb * kTcKBlock, row, k,
+              tma_load_3d(as + (size_t)(a_off[l] + row) * kTcKBlock * 2, &tm_a.m[sz][l], kb * kTcKBlock, row, k,
                           &full_bar[s]);
               row += rows;
             }
@@ -161,14 +189,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) {
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % p.stages;
-        if (!mbar_wait_or_fail(&full_bar[s], (kb / p.stages) & 1, &fail_sh)) {
+        const int s = kb % stages;
+        if (!mbar_wait_or_fail(&full_bar[s], (kb / stages) & 1, &fail_sh)) {
           fail_sh = 1;
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t xa = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const uint32_t xa = smem_u32(smem + (size_t)s * stage_bytes);
         const uint32_t aa = xa + kXStageBytes;
 #pragma unroll
         for (int l = 0; l < LORA_MAX_LANES; ++l) {
@@ -177,7 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
             const uint64_t ad = smem_desc(xa + 32 * kk, 16, 1024, kSwz128);
-            const uint64_t bd = smem_desc(aa + l * p.R16 * kTcKBlock * 2 + 32 * kk, 16, 1024, kSwz128);
+            const uint64_t bd = smem_desc(aa + a_off[l] * kTcKBlock * 2 + 32 * kk, 16, 1024, kSwz128);
             mma_bf16(tmem + (uint32_t)(l * p.R16), ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
         }
@@ -186,26 +214,141 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (ok) mma_commit(&done_bar);
     }
   } else {
+    // ---------------- epilogue, one tile row per thread
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int t = rb + row;
     const bool valid = t < re;
-    const bool ok = mbar_wait_or_fail(&done_bar, 0, &fail_sh);
-    if (!ok) fail_sh = 1;
+    bool ok = true;
+    if (nkb > 0) {  // an empty K range (d_in of one k-block) contributes zeros
+      ok = mbar_wait_or_fail(&done_bar, 0, &fail_sh);
+      if (!ok) fail_sh = 1;
+      else tc_fence_after();
+    }
+    // This K range's partial of the tile goes to u_tc, laid out per tile as
+    // [lane][column quad][row] float4 so that a warp's stores (and the last
+    // CTA's loads) cover 512 contiguous bytes.
+    const uint32_t trow = (uint32_t)(quad * 32) << 16;
+    auto part = [&](int ks, int l) {
+      return reinterpret_cast<float4*>(p.u_tc + ks * p.u_split_stride) +
+             ((size_t)tile * p.L + l) * (p.R16 / 4) * kTcTile + row;
+    };
     if (ok) {
-      tc_fence_after();
 #pragma unroll
       for (int l = 0; l < LORA_MAX_LANES; ++l) {
-        for (int q = 0; q < r16[l] / 16; ++q) {
-          float v[16];
-          tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(l * p.R16 + 16 * q), v);
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(p.u_tc + ksplit * p.u_split_stride +
-                                                    ((size_t)t * p.L + l) * p.R16 + 16 * q);
-            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-            dst[2] = make_float4(v[8], v[9], v[10], v[11]);
-            dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+        float4* dst = part(ksplit, l);
+        for (int c0 = 0; c0 < r16[l]; c0 += 64) {
+          const int ncol = min(64, r16[l] - c0);  // a multiple of 16
+          uint32_t v[4][16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (16 * q < ncol) {
+              if (nkb > 0) {
+                tmem_ld16_nowait(tmem + trow + (uint32_t)(l * p.R16 + c0 + 16 * q), v[q]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[q][e] = 0u;
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (16 * q < ncol) {
+              if (nkb > 0) tmem_wait_ld16(v[q]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[(size_t)((c0 + 16 * q) / 4 + e) * kTcTile] =
+                    make_float4(__uint_as_float(v[q][4 * e]), __uint_as_float(v[q][4 * e + 1]),
+                                __uint_as_float(v[q][4 * e + 2]), __uint_as_float(v[q][4 * e + 3]));
+            }
+          }
+        }
+      }
+    }
+    // Every CTA that got this far counts itself in, failed or not, so the
+    // counts stay whole; the one that completes the count resets it.
+    __threadfence();
+    named_bar_sync(1, 4 * 32);
+    if (warp == 2 && lane == 0) {
+      const int before = atomicAdd(&p.tile_cnt[tile], 1);
+      last_sh = before == kTcKSplit - 1;
+      if (last_sh) p.tile_cnt[tile] = 0;
+    }
+    named_bar_sync(1, 4 * 32);
+    if (last_sh) {
+      __threadfence();
+      // U = partial 0 + partial 1 + ... (K order; this CTA's own partial
+      // comes from TMEM, the others from L2), split into bf16 hi and lo and
+      // stored in the expand's K-major core-matrix layout: row m, rank
+      // columns 8g..8g+7 at (m / 8) * (r16 * 16) + g * 128 + (m % 8) * 16.
+#pragma unroll
+      for (int l = 0; l < LORA_MAX_LANES; ++l) {
+        if (r16[l] == 0) continue;
+        uint8_t* hi = reinterpret_cast<uint8_t*>(p.u_fmt + ((size_t)tile * p.L + l) * 2 * kTcTile * p.R16);
+        uint8_t* lo = hi + (size_t)kTcTile * r16[l] * 2;
+        const size_t sbo = (size_t)r16[l] * 16;
+        for (int c0 = 0; c0 < r16[l]; c0 += 64) {
+          const int ncol = min(64, r16[l] - c0);  // a multiple of 16
+          float4 oth[kTcKSplit - 1][16];         // every load of this batch is issued before the sums
+#pragma unroll
+          for (int j = 0; j < kTcKSplit - 1; ++j) {
+            const float4* src = part(j < ksplit ? j : j + 1, l) + (size_t)(c0 / 4) * kTcTile;
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+              oth[j][v] = 4 * v < ncol ? __ldcg(src + (size_t)v * kTcTile) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          uint32_t own[4][16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (16 * q < ncol) {
+              if (nkb > 0) {
+                tmem_ld16_nowait(tmem + trow + (uint32_t)(l * p.R16 + c0 + 16 * q), own[q]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) own[q][e] = 0u;
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (16 * q < ncol) {
+              if (nkb > 0) tmem_wait_ld16(own[q]);
+              float u[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float acc = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < kTcKSplit; ++ks) {
+                  float val;
+                  if (ks == ksplit) {
+                    val = __uint_as_float(own[q][e]);
+                  } else {
+                    const float4 w = oth[ks < ksplit ? ks : ks - 1][4 * q + e / 4];
+                    val = (e & 3) == 0 ? w.x : (e & 3) == 1 ? w.y : (e & 3) == 2 ? w.z : w.w;
+                  }
+                  acc = ks == 0 ? val : acc + val;
+                }
+                u[e] = valid ? acc : 0.f;
+              }
+#pragma unroll
+              for (int g = 0; g < 2; ++g) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float u0 = u[8 * g + 2 * e], u1 = u[8 * g + 2 * e + 1];
+                  const __nv_bfloat16 h0 = __float2bfloat16_rn(u0);
+                  const __nv_bfloat16 h1 = __float2bfloat16_rn(u1);
+                  const __nv_bfloat16 l0 = __float2bfloat16_rn(u0 - __bfloat162float(h0));
+                  const __nv_bfloat16 l1 = __float2bfloat16_rn(u1 - __bfloat162float(h1));
+                  hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                  lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                }
+                const int kg = (c0 + 16 * q) / 8 + g;
+                const size_t o = (size_t)(row >> 3) * sbo + (size_t)kg * 128 + (size_t)(row & 7) * 16;
+                *reinterpret_cast<uint4*>(hi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(lo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+              }
+            }
           }
         }
       }
@@ -235,7 +378,7 @@ constexpr int kRmwRowsPerWarp = kTcTile / kExpRmwWarps;  // 16
 __global__ void __launch_bounds__(kExpThreads, 1)
     tc_expand_kernel(const __grid_constant__ TmapSized tm_b, TcExpandParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bfull[2], bempty[2], afull[2], aempty[2], sfull[2], sempty[2];
+  __shared__ __align__(8) uint64_t bfull[2], bempty[2], afull[2], aempty[2], sfull[2], sempty[2], ufull;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int fail_sh;
 
@@ -245,8 +388,18 @@ __global__ void __launch_bounds__(kExpThreads, 1)
   if (tile >= p.counts[3]) return;
   const int q = item - tile * p.total_ng;
   int l = 0;
-  while (l + 1 < p.L && q >= p.ng_base[l + 1]) ++l;
-  const int ng = q - p.ng_base[l];
+  // lane of this item, and its column range, picked with constant indexes
+  // (a parameter array indexed at run time would be copied to local memory)
+  int ng = q, d_out_l = p.d_out[0], off_l = p.off[0];
+#pragma unroll
+  for (int i = 1; i < LORA_MAX_LANES; ++i) {
+    if (i < p.L && q >= p.ng_base[i]) {
+      l = i;
+      ng = q - p.ng_base[i];
+      d_out_l = p.d_out[i];
+      off_l = p.off[i];
+    }
+  }
   const int4 wk = p.work[tile];
   const int k = wk.x, rb = wk.y, re = wk.z;
   const int r = p.rank_tab[k * p.L + l];
@@ -254,7 +407,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
   const int r16 = (r + 15) & ~15;
   const int nk = r16 / 16;
   const int n_begin = ng * kTcNGroup;
-  const int n_end = min(p.d_out[l], n_begin + kTcNGroup);
+  const int n_end = min(d_out_l, n_begin + kTcNGroup);
   const int nchunks = (n_end - n_begin + kTcNT - 1) / kTcNT;
   const float sc = p.scale_tab[k * p.L + l];
 
@@ -264,7 +417,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
   uint8_t* bst = smem + 2 * kHalfBytes;
   const size_t bstage_bytes = (size_t)p.R16 * kTcNT * 2;
   uint8_t* uhi = bst + 2 * bstage_bytes;
-  uint8_t* ulo = uhi + (size_t)kTcTile * p.R16 * 2;
+  uint8_t* ulo = uhi + (size_t)kTcTile * r16 * 2;  // the shrink stores hi and lo back to back
   const uint32_t u_sbo = (uint32_t)(r16 / 8) * 128;  // bytes between 8-row groups of U
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -277,6 +430,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
       mbar_init(&sfull[s], kExpTmemWarps);
       mbar_init(&sempty[s], kExpRmwWarps);
     }
+    mbar_init(&ufull, 1);
     fail_sh = 0;
     fence_mbar_init();
   }
@@ -288,50 +442,12 @@ __global__ void __launch_bounds__(kExpThreads, 1)
   __syncthreads();  // barriers initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  // U rows -> bf16 hi / lo halves in the K-major core-matrix layout (the B
-  // tiles are already on their way meanwhile; the MMA warp waits on a named
-  // barrier for these halves only).
-  if (warp >= 2 && warp < 2 + kExpTmemWarps) {
-    const int m = (warp & 3) * 32 + lane;
-    const int t = rb + m;
-    const bool valid = t < re;
-    const float* urow = p.u_tc + ((size_t)t * p.L + l) * p.R16;
-    for (int kg = 0; kg < r16 / 8; ++kg) {
-      float u[8];
-      if (valid) {
-        const float4 a = *reinterpret_cast<const float4*>(urow + 8 * kg);
-        const float4 b = *reinterpret_cast<const float4*>(urow + 8 * kg + 4);
-        u[0] = a.x; u[1] = a.y; u[2] = a.z; u[3] = a.w; u[4] = b.x; u[5] = b.y; u[6] = b.z; u[7] = b.w;
-#pragma unroll
-        for (int ks = 1; ks < kTcKSplit; ++ks) {  // K-range partials, in order
-          const float4 c = *reinterpret_cast<const float4*>(urow + ks * p.u_split_stride + 8 * kg);
-          const float4 d = *reinterpret_cast<const float4*>(urow + ks * p.u_split_stride + 8 * kg + 4);
-          u[0] += c.x; u[1] += c.y; u[2] += c.z; u[3] += c.w; u[4] += d.x; u[5] += d.y; u[6] += d.z; u[7] += d.w;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] = 0.f;
-      }
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(u[2 * e]);
-        const __nv_bfloat16 h1 = __float2bfloat16_rn(u[2 * e + 1]);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(u[2 * e] - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(u[2 * e + 1] - __bfloat162float(h1));
-        hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-      }
-      const size_t o = (size_t)(m >> 3) * u_sbo + (size_t)kg * 128 + (size_t)(m & 7) * 16;
-      *reinterpret_cast<uint4*>(uhi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(ulo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 32 + kExpTmemWarps * 32);
-  }
-
   if (warp == 0) {
     if (lane == 0) {
+      // U of this tile and lane (bf16 hi and lo, written by the shrink) in one bulk copy
+      const uint32_t u_bytes = (uint32_t)kTcTile * r16 * 2 * 2;
+      mbar_expect_tx(&ufull, u_bytes);
+      bulk_load(uhi, p.u_fmt + ((size_t)tile * p.L + l) * 2 * kTcTile * p.R16, u_bytes, &ufull);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
         if (c >= 2) {
@@ -355,10 +471,11 @@ __global__ void __launch_bounds__(kExpThreads, 1)
       }
     }
   } else if (warp == 1) {
-    named_bar_sync(1, 32 + kExpTmemWarps * 32);  // U halves written
     if (lane == 0) {
       const uint32_t uh = smem_u32(uhi), ul = smem_u32(ulo);
-      for (int c = 0; c < nchunks; ++c) {
+      const bool u_ok = mbar_wait_or_fail(&ufull, 0, &fail_sh);
+      if (!u_ok) fail_sh = 1;
+      for (int c = 0; c < nchunks && u_ok; ++c) {
         const int s = c & 1;
         if (!mbar_wait_or_fail(&bfull[s], (c >> 1) & 1, &fail_sh)) {
           fail_sh = 1;
@@ -435,10 +552,12 @@ __global__ void __launch_bounds__(kExpThreads, 1)
     int total_h = 0;
     for (int c = 0; c < nchunks; ++c) total_h += min(kTcNT, n_end - (n_begin + c * kTcNT)) / kHalfCols;
     auto col_of = [&](int hidx) {  // first column of half chunk hidx (halves never straddle chunks)
-      return p.off[l] + n_begin + hidx * kHalfCols + 4 * chunk;
+      return off_l + n_begin + hidx * kHalfCols + 4 * chunk;
     };
-    // y of the next two half chunks is in flight while the current one is added
-    float4 yv[kRmwRowsPerWarp / 2], yn[kRmwRowsPerWarp / 2], ynn[kRmwRowsPerWarp / 2];
+    // Two half chunks of y in flight per warp: the one being added and the
+    // next; a half's buffer is refilled with the half two ahead as soon as it
+    // has been added (two named arrays, so they stay in registers).
+    float4 ya[kRmwRowsPerWarp / 2], yb[kRmwRowsPerWarp / 2];
     auto load_half = [&](int hidx, float4 (&dst)[kRmwRowsPerWarp / 2]) {
       const int col = col_of(hidx);
 #pragma unroll
@@ -448,14 +567,11 @@ __global__ void __launch_bounds__(kExpThreads, 1)
         if (t < re) dst[it] = *reinterpret_cast<const float4*>(p.y + (size_t)t * p.ldy + col);
       }
     };
-    if (total_h > 0) load_half(0, yv);
-    if (total_h > 1) load_half(1, yn);
-    for (int hh = 0; hh < total_h; ++hh) {
+    auto add_half = [&](int hh, float4 (&yc)[kRmwRowsPerWarp / 2]) -> bool {
       const int sb = hh & 1;
-      if (hh + 2 < total_h) load_half(hh + 2, ynn);
       if (!mbar_wait_or_fail(&sfull[sb], (hh >> 1) & 1, &fail_sh)) {
         fail_sh = 1;
-        break;
+        return false;
       }
       const uint8_t* st = ystage + (size_t)sb * kHalfBytes;
       const int col = col_of(hh);
@@ -466,7 +582,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
         if (t < re) {
           const float4 d = *reinterpret_cast<const float4*>(st + (size_t)row * (kHalfCols * 4) +
                                                             ((chunk ^ (row & 15)) * 16));
-          float4 a = yv[it];
+          float4 a = yc[it];
           a.x += d.x;
           a.y += d.y;
           a.z += d.z;
@@ -476,11 +592,14 @@ __global__ void __launch_bounds__(kExpThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
-#pragma unroll
-      for (int it = 0; it < kRmwRowsPerWarp / 2; ++it) {
-        yv[it] = yn[it];
-        yn[it] = ynn[it];
-      }
+      if (hh + 2 < total_h) load_half(hh + 2, yc);
+      return true;
+    };
+    if (total_h > 0) load_half(0, ya);
+    if (total_h > 1) load_half(1, yb);
+    for (int hh = 0; hh < total_h; hh += 2) {
+      if (!add_half(hh, ya)) break;
+      if (hh + 1 < total_h && !add_half(hh + 1, yb)) break;
     }
   }
   tc_fence_before();
@@ -523,21 +642,22 @@ int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint
   p.work = seg->tc_work;
   p.rank_tab = pool->rank_tab;
   p.u_tc = pool->u_tc;
+  p.u_fmt = pool->u_fmt;
+  p.tile_cnt = pool->tile_cnt;
   p.status = seg->status;
   p.L = pool->L;
   p.R16 = pool->R16;
   p.num_kb = pool->d_in / kTcKBlock;
-  p.u_split_stride = (size_t)pool->max_tokens * pool->L * pool->R16;
-  p.stage_bytes = kXStageBytes + pool->L * pool->R16 * kTcKBlock * 2;
-  // two CTAs per SM: each keeps its ring within ~100 KB of shared memory
-  int stages = (100 * 1024) / p.stage_bytes;
-  if (stages > 6) stages = 6;
-  if (stages < 2) stages = 2;
-  p.stages = stages;
+  p.tiles_cap = tc_tile_cap(pool->max_tokens);
+  p.u_split_stride = (size_t)p.tiles_cap * pool->L * pool->R16 * kTcTile;
+  // Two CTAs per SM: each keeps its ring within ~100 KB of shared memory (at
+  // least two stages of the largest kind: every lane at R16).
+  const int max_stage = kXStageBytes + pool->L * pool->R16 * kTcKBlock * 2;
+  p.ring_bytes = 100 * 1024 > 2 * max_stage ? 100 * 1024 : 2 * max_stage;
   int cols = 32;
   while (cols < pool->L * pool->R16) cols <<= 1;
   p.tmem_cols = cols;
-  const int smem = stages * p.stage_bytes + 1024;
+  const int smem = p.ring_bytes + 1024;
   if (!set_smem_limit(reinterpret_cast<const void*>(tc_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   tc_shrink_kernel<<<grid, kTcThreads, smem, st>>>(tm_x128, tm_x32, pool->tm_a, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -559,8 +679,7 @@ int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, 
   p.work = seg->tc_work;
   p.rank_tab = pool->rank_tab;
   p.scale_tab = pool->scale_tab;
-  p.u_tc = pool->u_tc;
-  p.u_split_stride = (size_t)pool->max_tokens * pool->L * pool->R16;
+  p.u_fmt = pool->u_fmt;
   p.y = y;
   p.ldy = ldy;
   p.status = seg->status;

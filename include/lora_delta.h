@@ -80,9 +80,10 @@ typedef struct lora_segments lora_segments;
  * lane, bf16 factors of a rank r <= max_rank padded with zeros to
  * R16 = max_rank rounded up to a multiple of 16, a rank and an fp32 scale
  * (the caller computes scale = lora_alpha / r * strength).  The pool also
- * holds the per-row fp32 rank-space scratch of up to max_tokens rows used
- * between the shrink and the expand kernels, so two applies on one pool must
- * be ordered on one stream.
+ * holds the rank-space scratch of up to max_tokens rows used between the
+ * shrink and the expand kernels (fp32 partial sums, bf16 U tiles, and per-tile
+ * counters that the zero fill starts at zero and every apply leaves at zero),
+ * so two applies on one pool must be ordered on one stream.
  *
  * Shapes: d_in and every lane_d_out[l] must be positive multiples of 64;
  * 1 <= num_lanes <= LORA_MAX_LANES; 2 <= num_slots <= LORA_MAX_SLOTS;
@@ -193,7 +194,8 @@ int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, co
 
 /* One kernel of lora_apply_shrink_expand, for per-kernel timing:
  * stage 1 = decode shrink, 2 = decode expand, 3 = tensor shrink, 4 = tensor
- * expand.  Running stages 1..4 in order is exactly lora_apply_shrink_expand. */
+ * expand.  Running stages 1..4 in order on one stream gives exactly the
+ * result of lora_apply_shrink_expand. */
 int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y,
                      int64_t ldx, int64_t ldy, int stage, lora_stream_t stream);
 
@@ -202,20 +204,22 @@ int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void
  * only its input and output buffers, or a serving loop whose memory plan is
  * frozen after start-up.  No passage of the pages has a counterpart; this is a
  * property of the library, not of the method.
- *   - The rank-space intermediate (decode partial sums and tensor-path rank
- *     rows, (C + 2) * T * num_lanes * R16 floats with C = ceil(d_in / 1024))
- *     lives in a fixed array compiled into the library, of
- *     LORA_NOALLOC_SCRATCH_BYTES; every GPU that loads the library holds it
- *     until the process exits.  A step that needs more returns LORA_ERR_SHAPE
- *     before anything is enqueued.
+ *   - The rank-space intermediate lives in a fixed array compiled into the
+ *     library, of LORA_NOALLOC_SCRATCH_BYTES; every GPU that loads the
+ *     library holds it until the process exits.  A step needs, in floats,
+ *     16384 (per-tile counters) + C * T * num_lanes * R16 (decode partial
+ *     sums, C = ceil(d_in / 1024)) + 3 * (T / 64 + 1) * num_lanes * R16 * 128
+ *     (tensor-path partial sums and U tiles); one that needs more returns
+ *     LORA_ERR_SHAPE before anything is enqueued.
  *   - The call allocates nothing.  Its first call on a device looks up the
  *     array's device address (cudaGetSymbolAddress) with that device current;
  *     make that first call before any stream capture.  The current device must
  *     be the pool's device (else LORA_ERR_ARG).
  *   - Every call shares the one array.  Each scratch word a call reads it has
- *     written earlier in the same call, so nothing needs clearing, but calls
- *     whose GPU work overlaps (other streams, other threads) race on it: order
- *     them on one stream.
+ *     written earlier in the same call, except the per-tile counters, which
+ *     start at zero and which every call leaves at zero; so nothing needs
+ *     clearing, but calls whose GPU work overlaps (other streams, other
+ *     threads) race on it: order them on one stream.
  * Arguments, results and other errors are those of lora_apply_shrink_expand. */
 #define LORA_NOALLOC_SCRATCH_BYTES (64u << 20)
 int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lora_segments* seg, const void* x,

@@ -48,6 +48,19 @@ def test_mixed_small_full_oracle(oracle_mod):
     _oracle_check(oracle_mod, wl, wl.projections[0], what="mixed")
 
 
+@pytest.mark.parametrize("d_in", [64, 192, 1088])
+def test_k_block_counts(oracle_mod, d_in):
+    # d_in of 1, 3 and 17 blocks of 64: the tensor shrink's two K ranges are
+    # empty / uneven, and 1088 also spans two decode K chunks of 1024
+    lens = [130, 1, 64, 3, 1, 77]
+    ids = [1, 2, 2, 1, 0, 3]
+    N = 4
+    rank = np.array([[0], [16], [40], [7]], dtype=np.int32)
+    wl = W.custom_workload(lens, ids, d_in=d_in, lane_d_out=[192], num_slots=N, max_rank=48, rank=rank,
+                           seed=d_in)
+    _oracle_check(oracle_mod, wl, wl.projections[0], what=f"d_in={d_in}")
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode_oproj"])
 def test_decode_configs_full(oracle_mod, name):
     wl = W.make_workload(name)

@@ -80,8 +80,6 @@ struct lora_segments {
   int32_t* status = nullptr;
   int32_t* counts = nullptr;
   int32_t* seq_start = nullptr;
-  int32_t* seq_pos = nullptr;
-  int32_t* seq_tile = nullptr;
   int32_t* slot = nullptr;
   int32_t* perm = nullptr;
   int32_t* seg_off = nullptr;

@@ -24,6 +24,8 @@ namespace lora {
 namespace {
 
 constexpr int kSegThreads = 1024;
+// Dynamic shared memory the builder may use (227 KB per block, less its static part).
+constexpr size_t kSegSmemLimit = 227 * 1024 - 2048;
 
 struct SegParams {
   const int32_t* ids;
@@ -32,8 +34,6 @@ struct SegParams {
   int32_t* status;
   int32_t* counts;
   int32_t* seq_start;
-  int32_t* seq_pos;
-  int32_t* seq_tile;
   int32_t* slot;
   int32_t* perm;
   int32_t* seg_off;
@@ -71,147 +71,152 @@ __device__ int block_exclusive_scan(int v, int* sums, int& total) {
   return ex;
 }
 
+// Three exclusive scans at once over arrays of n0, n1, n2 ints in shared
+// memory (in place: each entry becomes the sum of the entries before it).
+// Each thread takes `per` consecutive entries of every array; the totals are
+// returned.  All threads call it; two barriers.
+__device__ void block_scan3(int* a0, int n0, int* a1, int n1, int* a2, int n2, int per, int (*sums)[33],
+                            int& t0, int& t1, int& t2) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lo = threadIdx.x * per;
+  int v0 = 0, v1 = 0, v2 = 0;
+  for (int i = 0; i < per; ++i) {
+    if (lo + i < n0) v0 += a0[lo + i];
+    if (lo + i < n1) v1 += a1[lo + i];
+    if (lo + i < n2) v2 += a2[lo + i];
+  }
+  int x0 = v0, x1 = v1, x2 = v2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y0 = __shfl_up_sync(0xffffffffu, x0, o);
+    const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
+    const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
+    if (lane >= o) {
+      x0 += y0;
+      x1 += y1;
+      x2 += y2;
+    }
+  }
+  if (lane == 31) {
+    sums[0][warp] = x0;
+    sums[1][warp] = x1;
+    sums[2][warp] = x2;
+  }
+  __syncthreads();
+  if (warp < 3) {
+    const int w = sums[warp][lane];
+    int x = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    sums[warp][lane] = x - w;
+    if (lane == 31) sums[warp][32] = x;
+  }
+  __syncthreads();
+  int c0 = sums[0][warp] + x0 - v0, c1 = sums[1][warp] + x1 - v1, c2 = sums[2][warp] + x2 - v2;
+  for (int i = 0; i < per; ++i) {
+    if (lo + i < n0) {
+      const int e = a0[lo + i];
+      a0[lo + i] = c0;
+      c0 += e;
+    }
+    if (lo + i < n1) {
+      const int e = a1[lo + i];
+      a1[lo + i] = c1;
+      c1 += e;
+    }
+    if (lo + i < n2) {
+      const int e = a2[lo + i];
+      a2[lo + i] = c2;
+      c2 += e;
+    }
+  }
+  t0 = sums[0][32];
+  t1 = sums[1][32];
+  t2 = sums[2][32];
+}
+
+// Shared memory of the builder, in ints: six per-sequence arrays of S and
+// the per-key tables (2N + 2N + N + (N + 1) + (N + 1)).
+size_t seg_smem_ints(int N, int S) { return 6 * (size_t)S + 7 * (size_t)N + 2; }
+
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) {
   extern __shared__ int smem_dyn[];
-  __shared__ int sums[33];
+  __shared__ int scan_sums[3][33];
   __shared__ long long warp_len[kSegThreads / 32];
+  __shared__ int warp_bad[kSegThreads / 32];
 
   const int N = p.N, S = p.S, T = p.T;
-  int* cnt_tok = smem_dyn;            // [2N]  rows per (class, slot)
-  int* tok_off = cnt_tok + 2 * N;     // [2N]  first perm position of (class, slot)
-  int* run_tok = tok_off + 2 * N;     // [2N]  running position while ranking sequences
-  int* cnt_tile = run_tok + 2 * N;    // [N]   class-1 tiles per slot
-  int* tc_base = cnt_tile + N;        // [N+1] first tile index per slot
-  int* run_tile = tc_base + N + 1;    // [N]
-  int* dec_base = run_tile + N;       // [N+1] first decode group per slot
+  int* s_len = smem_dyn;           // [S] q_len
+  int* s_id = s_len + S;           // [S] slot
+  int* s_start = s_id + S;         // [S] first row
+  int* s_pos = s_start + S;        // [S] rank of the first row inside its (class, slot) bin
+  int* s_tile = s_pos + S;         // [S] rank of the first tile inside its slot's tiles
+  int* s_key = s_tile + S;         // [S] (class, slot) key, -1 if the sequence is inactive; bit 30: last of
+                                   //     its key in its warp
+  int* cnt_tok = s_key + S;        // [2N] rows per (class, slot), then their first perm position
+  int* run_tok = cnt_tok + 2 * N;  // [2N] running position while ranking sequences
+  int* cnt_tile = run_tok + 2 * N; // [N]  class-1 tiles per slot, then the first tile index
+  int* dec_cnt = cnt_tile + N;     // [N+1] decode groups per slot, then the first group index
+  int* tc_cnt = dec_cnt + N + 1;   // [N+1] class-1 tiles per slot (scan input), then the first tile
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kLastBit = 1 << 30;
 
-  // ---- validation (block reductions, no contended atomics)
-  for (int i = tid; i < 2 * N; i += kSegThreads) cnt_tok[i] = 0;
+  // ---- load the sequences once; validation by block reductions
+  for (int i = tid; i < 2 * N; i += kSegThreads) run_tok[i] = 0;
   for (int i = tid; i < N; i += kSegThreads) cnt_tile[i] = 0;
   long long my_sum = 0;
-  int my_bad_len = 0, my_bad_id = 0;
+  int my_bad = 0;  // bit 0: a negative length, bit 1: an id out of range
   for (int s = tid; s < S; s += kSegThreads) {
     const int len = p.lens[s], id = p.ids[s];
-    my_bad_len |= len < 0;
-    my_bad_id |= (id < 0 || id >= N);
+    s_len[s] = len;
+    s_id[s] = id;
+    my_bad |= (len < 0 ? 1 : 0) | ((id < 0 || id >= N) ? 2 : 0);
     my_sum += len;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) my_sum += __shfl_xor_sync(0xffffffffu, my_sum, o);
-  if (lane == 0) warp_len[warp] = my_sum;
-  const int bad_len = __syncthreads_or(my_bad_len);
-  const int bad_id = __syncthreads_or(my_bad_id);
-  long long total_len = 0;
-#pragma unroll 8
-  for (int w = 0; w < kSegThreads / 32; ++w) total_len += warp_len[w];
-  if (bad_len || total_len != (long long)T || bad_id) {
+  for (int o = 16; o > 0; o >>= 1) {
+    my_sum += __shfl_xor_sync(0xffffffffu, my_sum, o);
+    my_bad |= __shfl_xor_sync(0xffffffffu, my_bad, o);
+  }
+  if (lane == 0) {
+    warp_len[warp] = my_sum;
+    warp_bad[warp] = my_bad;
+  }
+  __syncthreads();
+  long long total_len = warp_len[lane];
+  int bad = warp_bad[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    total_len += __shfl_xor_sync(0xffffffffu, total_len, o);
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  if ((bad & 1) || total_len != (long long)T || (bad & 2)) {
     if (tid < 4) p.counts[tid] = 0;
-    if (tid == 0) *p.status = (bad_len || total_len != (long long)T) ? LORA_ERR_META : LORA_ERR_SLOT;
+    if (tid == 0) *p.status = ((bad & 1) || total_len != (long long)T) ? LORA_ERR_META : LORA_ERR_SLOT;
     return;
   }
 
-  // ---- seq_start = exclusive prefix of the lengths
+  // ---- per sequence: first row (block scan), key, and its rank among the
+  // earlier lanes of its warp with the same key (rows and tiles)
   int carry = 0;
   for (int b = 0; b < S; b += kSegThreads) {
     const int s = b + tid;
-    const int v = s < S ? p.lens[s] : 0;
-    int tot;
-    const int ex = block_exclusive_scan(v, sums, tot);
-    if (s < S) p.seq_start[s] = carry + ex;
-    carry += tot;
-  }
-  if (tid == 0) p.seq_start[S] = T;
-
-  // ---- histogram of rows per (class, slot) and class-1 tiles per slot; lanes
-  // with the same key add up first, so each warp issues one atomic per key
-  for (int b = 0; b < S; b += kSegThreads) {
-    const int s = b + tid;
-    int key = -1, len = 0, nt = 0, id = 0;
+    int key = -1, len = 0, nt = 0;
     if (s < S) {
-      len = p.lens[s];
-      id = p.ids[s];
+      len = s_len[s];
+      const int id = s_id[s];
       if (id != 0 && len > 0) {
         const int cls = len >= LORA_TC_MIN_QLEN ? 1 : 0;
         key = cls * N + id;
         nt = cls ? (len + kTcTile - 1) / kTcTile : 0;
       }
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int leader = __ffs(peers) - 1;
-    int gl = 0, gt = 0;
-    for (unsigned m = peers; m; m &= m - 1) {
-      const int j = __ffs(m) - 1;
-      gl += __shfl_sync(peers, len, j);
-      gt += __shfl_sync(peers, nt, j);
-    }
-    if (key >= 0 && lane == leader) {
-      atomicAdd(&cnt_tok[key], gl);
-      if (gt) atomicAdd(&cnt_tile[id], gt);
-    }
-  }
-  __syncthreads();
-
-  // ---- offsets: rows (class-major), decode groups per slot, tiles per slot
-  int n_active, n_dec_work, n_tc;
-  carry = 0;
-  for (int b = 0; b < 2 * N; b += kSegThreads) {
-    const int key = b + tid;
-    const int v = key < 2 * N ? cnt_tok[key] : 0;
     int tot;
-    const int ex = block_exclusive_scan(v, sums, tot);
-    if (key < 2 * N) tok_off[key] = carry + ex;
-    carry += tot;
-  }
-  n_active = carry;
-  carry = 0;
-  for (int b = 0; b < N; b += kSegThreads) {
-    const int k = b + tid;
-    const int v = k < N ? (cnt_tok[k] + kDecGroup - 1) / kDecGroup : 0;
-    int tot;
-    const int ex = block_exclusive_scan(v, sums, tot);
-    if (k < N) dec_base[k] = carry + ex;
-    carry += tot;
-  }
-  n_dec_work = carry;
-  carry = 0;
-  for (int b = 0; b < N; b += kSegThreads) {
-    const int k = b + tid;
-    const int v = k < N ? cnt_tile[k] : 0;
-    int tot;
-    const int ex = block_exclusive_scan(v, sums, tot);
-    if (k < N) tc_base[k] = carry + ex;
-    carry += tot;
-  }
-  n_tc = carry;
-  if (tid == 0) {
-    dec_base[N] = n_dec_work;
-    tc_base[N] = n_tc;
-  }
-  for (int key = tid; key < 2 * N; key += kSegThreads) run_tok[key] = tok_off[key];
-  for (int k = tid; k < N; k += kSegThreads) run_tile[k] = tc_base[k];
-  for (int i = tid; i < 2 * (N + 1); i += kSegThreads) {
-    const int c = i / (N + 1), k = i % (N + 1);
-    p.seg_off[i] = (k < N) ? tok_off[c * N + k] : (c == 0 ? tok_off[N] : n_active);
-  }
-  __syncthreads();
-
-  // ---- stable rank of each active sequence inside its (class, slot) bin.
-  // Sequences are visited in index order: chunk by chunk, warp by warp; inside
-  // a warp the lanes with the same key take exclusive prefixes of their lengths.
-  for (int b = 0; b < S; b += kSegThreads) {
-    const int s = b + tid;
-    int key = -1, len = 0, nt = 0, id = 0;
-    if (s < S) {
-      len = p.lens[s];
-      id = p.ids[s];
-      if (id != 0 && len > 0) {
-        const int cls = len >= LORA_TC_MIN_QLEN ? 1 : 0;
-        key = cls * N + id;
-        nt = cls ? (len + kTcTile - 1) / kTcTile : 0;
-      }
-    }
+    const int ex = block_exclusive_scan(s < S ? len : 0, scan_sums[0], tot);
     int pl = 0, pt = 0;
     bool last = true;
 #pragma unroll 4
@@ -228,58 +233,100 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
         }
       }
     }
-    const int nwarps = min(32, (S - b + 31) / 32);
-    for (int w = 0; w < nwarps; ++w) {
-      __syncthreads();
-      if (warp == w) {
-        int base_tok = 0, base_tile = 0;
-        if (key >= 0) {
-          base_tok = run_tok[key];
-          if (nt) base_tile = run_tile[id];
-        }
-        __syncwarp();
-        if (key >= 0) {
-          if (last) {
-            run_tok[key] = base_tok + pl + len;
-            if (nt) run_tile[id] = base_tile + pt + nt;
-          }
-          p.seq_pos[s] = base_tok + pl;
-          p.seq_tile[s] = base_tile + pt;
+    if (s < S) {
+      s_start[s] = carry + ex;
+      p.seq_start[s] = carry + ex;
+      s_pos[s] = pl;
+      s_tile[s] = pt;
+      s_key[s] = key < 0 ? -1 : (key | (last ? kLastBit : 0));
+    }
+    carry += tot;
+  }
+  if (tid == 0) p.seq_start[S] = T;
+  __syncthreads();
+
+  // ---- stable ranks: one warp walks the sequences 32 at a time in index
+  // order; the per-key running counts end as the rows per (class, slot) and
+  // the tiles per slot
+  if (warp == 0) {
+    for (int b = 0; b < S; b += 32) {
+      const int s = b + lane;
+      const int kk = s < S ? s_key[s] : -1;
+      const int key = kk < 0 ? -1 : (kk & (kLastBit - 1));
+      const int id = key < 0 ? 0 : (key >= N ? key - N : key);
+      const bool tc = key >= N;
+      int base_tok = 0, base_tile = 0;
+      if (key >= 0) {
+        base_tok = run_tok[key];
+        if (tc) base_tile = cnt_tile[id];
+      }
+      __syncwarp();
+      if (key >= 0) {
+        const int pl = s_pos[s], pt = s_tile[s];
+        s_pos[s] = base_tok + pl;
+        if (tc) s_tile[s] = base_tile + pt;
+        if (kk & kLastBit) {
+          run_tok[key] = base_tok + pl + s_len[s];
+          if (tc) cnt_tile[id] = base_tile + pt + (s_len[s] + kTcTile - 1) / kTcTile;
         }
       }
+      __syncwarp();
     }
   }
   __syncthreads();
 
+  // ---- offsets: rows (class-major), decode groups per slot, tiles per slot
+  for (int i = tid; i < 2 * N; i += kSegThreads) cnt_tok[i] = run_tok[i];
+  for (int k = tid; k < N; k += kSegThreads) {
+    dec_cnt[k] = (run_tok[k] + kDecGroup - 1) / kDecGroup;
+    tc_cnt[k] = cnt_tile[k];
+  }
+  __syncthreads();
+  int n_active, n_dec_work, n_tc;
+  block_scan3(cnt_tok, 2 * N, dec_cnt, N, tc_cnt, N, (2 * N + kSegThreads - 1) / kSegThreads, scan_sums, n_active,
+              n_dec_work, n_tc);
+  if (tid == 0) {
+    dec_cnt[N] = n_dec_work;
+    tc_cnt[N] = n_tc;
+  }
+  __syncthreads();
+  // cnt_tok = first perm position of each (class, slot); run_tok = its rows
+  for (int i = tid; i < 2 * (N + 1); i += kSegThreads) {
+    const int c = i / (N + 1), k = i % (N + 1);
+    p.seg_off[i] = (k < N) ? cnt_tok[c * N + k] : (c == 0 ? cnt_tok[N] : n_active);
+  }
+
   // ---- per-token slot and perm: one warp per sequence, coalesced writes
   for (int s = warp; s < S; s += kSegThreads / 32) {
-    const int id = p.ids[s], st = p.seq_start[s], len = p.lens[s];
-    const int pos = id != 0 ? p.seq_pos[s] : 0;
+    const int id = s_id[s], st = s_start[s], len = s_len[s];
+    const int kk = s_key[s];
+    const int pos = kk < 0 ? 0 : cnt_tok[kk & (kLastBit - 1)] + s_pos[s];
     for (int j = lane; j < len; j += 32) {
       p.slot[st + j] = id;
-      if (id != 0) p.perm[pos + j] = st + j;
+      if (kk >= 0) p.perm[pos + j] = st + j;
     }
   }
 
   // ---- decode groups: slot k's class-0 run cut into runs of <= kDecGroup
   for (int w = tid; w < n_dec_work; w += kSegThreads) {
-    int lo = 0, hi = N - 1;  // last k with dec_base[k] <= w
+    int lo = 0, hi = N - 1;  // last k with dec_cnt[k] <= w
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
-      if (dec_base[mid] <= w) lo = mid; else hi = mid - 1;
+      if (dec_cnt[mid] <= w) lo = mid; else hi = mid - 1;
     }
     const int k = lo;
-    const int gi = w - dec_base[k];
-    const int pb = tok_off[k] + gi * kDecGroup;
-    const int pe = min(pb + kDecGroup, tok_off[k] + cnt_tok[k]);
+    const int gi = w - dec_cnt[k];
+    const int pb = cnt_tok[k] + gi * kDecGroup;
+    const int pe = min(pb + kDecGroup, cnt_tok[k] + run_tok[k]);
     p.dec_work[w] = make_int4(k, pb, pe, 0);
   }
 
   // ---- tensor tiles: each class-1 sequence cut into tiles of <= kTcTile rows
   for (int s = tid; s < S; s += kSegThreads) {
-    const int len = p.lens[s], id = p.ids[s];
-    if (id != 0 && len >= LORA_TC_MIN_QLEN) {
-      const int st = p.seq_start[s], base = p.seq_tile[s];
+    const int kk = s_key[s];
+    if (kk >= 0 && (kk & (kLastBit - 1)) >= N) {
+      const int id = s_id[s], st = s_start[s], len = s_len[s];
+      const int base = tc_cnt[id] + s_tile[s];
       for (int i = 0, rb = st; rb < st + len; ++i, rb += kTcTile)
         p.tc_work[base + i] = make_int4(id, rb, min(rb + kTcTile, st + len), s);
     }
@@ -287,16 +334,12 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
 
   if (tid == 0) {
     p.counts[0] = n_active;
-    p.counts[1] = tok_off[N];
+    p.counts[1] = cnt_tok[N];
     p.counts[2] = n_dec_work;
     p.counts[3] = n_tc;
     *p.status = LORA_OK;
   }
 }
-
-// Dynamic shared memory of seg_build_kernel: cnt_tok, tok_off, run_tok (2N
-// each), cnt_tile (N), tc_base (N+1), run_tile (N), dec_base (N+1).
-size_t seg_smem_bytes(int N) { return sizeof(int) * (size_t)(3 * 2 * N + N + (N + 1) + N + (N + 1)); }
 
 }  // namespace
 
@@ -311,14 +354,12 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
   p.status = seg->status;
   p.counts = seg->counts;
   p.seq_start = seg->seq_start;
-  p.seq_pos = seg->seq_pos;
-  p.seq_tile = seg->seq_tile;
   p.slot = seg->slot;
   p.perm = seg->perm;
   p.seg_off = seg->seg_off;
   p.dec_work = seg->dec_work;
   p.tc_work = seg->tc_work;
-  const size_t sm = seg_smem_bytes(seg->N);
+  const size_t sm = sizeof(int) * seg_smem_ints(seg->N, S);
   if (sm > 48 * 1024 && !set_smem_limit(reinterpret_cast<const void*>(seg_build_kernel), seg->device, (int)sm))
     return LORA_ERR_CUDA;
   seg_build_kernel<<<1, kSegThreads, sm, st>>>(p);
@@ -333,7 +374,7 @@ using namespace lora;
 namespace {
 
 struct SegLayout {
-  size_t status, counts, seq_start, seq_pos, seq_tile, slot, perm, seg_off, dec_work, tc_work, total;
+  size_t status, counts, seq_start, slot, perm, seg_off, dec_work, tc_work, total;
   int cap_dec, cap_tc;
 };
 
@@ -341,14 +382,14 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 bool seg_layout(int max_seqs, int max_tokens, int N, SegLayout* L) {
   if (max_seqs < 1 || max_tokens < 1 || N < 2 || N > LORA_MAX_SLOTS) return false;
+  // the builder keeps every sequence and every slot's counters in shared memory
+  if (sizeof(int) * seg_smem_ints(N, max_seqs) > kSegSmemLimit) return false;
   L->cap_dec = ceil_div(max_tokens, kDecGroup) + N;
   L->cap_tc = ceil_div(max_tokens, kTcTile) + max_seqs;
   size_t o = 0;
   L->status = o; o += 64;
   L->counts = o; o = align256(o + 64);
   L->seq_start = o; o = align256(o + 4 * (size_t)(max_seqs + 1));
-  L->seq_pos = o; o = align256(o + 4 * (size_t)max_seqs);
-  L->seq_tile = o; o = align256(o + 4 * (size_t)max_seqs);
   L->slot = o; o = align256(o + 4 * (size_t)max_tokens);
   L->perm = o; o = align256(o + 4 * (size_t)max_tokens);
   L->seg_off = o; o = align256(o + 4 * (size_t)(2 * (N + 1)));
@@ -389,8 +430,6 @@ int lora_segments_create(lora_segments** out, void* dev_ws, size_t ws_bytes, int
   s->status = reinterpret_cast<int32_t*>(b + L.status);
   s->counts = reinterpret_cast<int32_t*>(b + L.counts);
   s->seq_start = reinterpret_cast<int32_t*>(b + L.seq_start);
-  s->seq_pos = reinterpret_cast<int32_t*>(b + L.seq_pos);
-  s->seq_tile = reinterpret_cast<int32_t*>(b + L.seq_tile);
   s->slot = reinterpret_cast<int32_t*>(b + L.slot);
   s->perm = reinterpret_cast<int32_t*>(b + L.perm);
   s->seg_off = reinterpret_cast<int32_t*>(b + L.seg_off);

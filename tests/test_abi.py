@@ -65,6 +65,11 @@ def test_segments_bytes(lib):
     assert LD.lora_segments_bytes(0, 16, 4) == 0
     assert LD.lora_segments_bytes(4, 16, 1) == 0
     assert LD.lora_segments_bytes(4, 16, 4097) == 0
+    # the builder holds 6 ints per sequence and 7 per slot (+2) in 227 KiB - 2 KiB of shared memory
+    assert LD.lora_segments_bytes(7210, 16, 2048) > 0
+    assert LD.lora_segments_bytes(7211, 16, 2048) == 0
+    assert LD.lora_segments_bytes(9523, 16, 65) > 0
+    assert LD.lora_segments_bytes(9524, 16, 65) == 0
 
 
 def test_host_argument_errors_need_no_gpu(lib):

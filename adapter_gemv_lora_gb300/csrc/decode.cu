@@ -69,6 +69,35 @@ struct DecParams {
   int nc_base[LORA_MAX_LANES + 1];
 };
 
+// Element l of a per-lane parameter array, read with constant indexes.
+template <typename V>
+__device__ __forceinline__ V lane_param(const V (&a)[LORA_MAX_LANES], int l) {
+  V v = a[0];
+#pragma unroll
+  for (int i = 1; i < LORA_MAX_LANES; ++i)
+    if (l == i) v = a[i];
+  return v;
+}
+
+// Lane, first column, width and y offset of expand column chunk q, picked with
+// constant indexes (a parameter array indexed at run time would be copied to
+// local memory).
+__device__ __forceinline__ void pick_lane(const DecParams& p, int q, int& l, int& n0, int& dout, int& off) {
+  l = 0;
+  n0 = q * kDecNChunk;
+  dout = p.d_out[0];
+  off = p.off[0];
+#pragma unroll
+  for (int i = 1; i < LORA_MAX_LANES; ++i) {
+    if (i < p.L && q >= p.nc_base[i]) {
+      l = i;
+      n0 = (q - p.nc_base[i]) * kDecNChunk;
+      dout = p.d_out[i];
+      off = p.off[i];
+    }
+  }
+}
+
 // One step of a butterfly reduce-scatter: lanes exchange half of their values
 // with lane ^ o and keep the sum of the half selected by bit o of their id.
 template <int HALF>
@@ -90,9 +119,11 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
   __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages], xfull[2], xempty[2];
   __shared__ int fail_sh;
 
-  if (*p.status != 0) return;
+  pdl_wait();  // the previous kernel's results are visible from here on
+  const int status = *p.status, n_groups = p.counts[2];  // both loads in flight together
+  if (status != 0) return;
   const int per_group = p.L * p.C;
-  const int n_items = p.counts[2] * per_group;
+  const int n_items = n_groups * per_group;
   if ((int)blockIdx.x >= n_items) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -129,13 +160,18 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
             fail_sh = 1;
             break;
           }
+          int row[kDecGroup];  // all row indexes first: the copies below are ordered memory operations
+#pragma unroll
+          for (int gg = 0; gg < kDecGroup; ++gg) row[gg] = gg < nrows ? p.perm[g.y + gg] : 0;
           mbar_expect_tx(&xfull[xs], (uint32_t)(nrows * klen * 2));
-          for (int gg = 0; gg < nrows; ++gg)
-            bulk_load(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk,
-                      p.x + (size_t)p.perm[g.y + gg] * p.ldx + k0, (uint32_t)(klen * 2), &xfull[xs]);
+#pragma unroll
+          for (int gg = 0; gg < kDecGroup; ++gg)
+            if (gg < nrows)
+              bulk_load(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk, p.x + (size_t)row[gg] * p.ldx + k0,
+                        (uint32_t)(klen * 2), &xfull[xs]);
           ++xj;
         }
-        const uint16_t* Ab = p.A[l] + (size_t)k * p.R16 * p.d_in + k0;
+        const uint16_t* Ab = lane_param(p.A, l) + (size_t)k * p.R16 * p.d_in + k0;
         for (int rb = 0; rb < r; rb += kShRows, ++fill) {
           const int s = fill % kShStages;
           if (fill >= kShStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kShStages) - 1) & 1, &fail_sh)) {
@@ -170,15 +206,23 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
         ok = false;
         fail_sh = 1;
       }
-      float xv[kDecGroup][8];
+      // x of rows 2p and 2p+1 side by side, for the packed fma
+      float2 xp[kDecGroup / 2][8];
 #pragma unroll
-      for (int gg = 0; gg < kDecGroup; ++gg) {
-        if (ok && gg < nrows && has_k) {
-          unpack8(*reinterpret_cast<const uint4*>(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk + kk), xv[gg]);
-        } else {
+      for (int pp = 0; pp < kDecGroup / 2; ++pp) {
+        float xv[2][8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) xv[gg][e] = 0.f;
+        for (int h = 0; h < 2; ++h) {
+          const int gg = 2 * pp + h;
+          if (ok && gg < nrows && has_k) {
+            unpack8(*reinterpret_cast<const uint4*>(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk + kk), xv[h]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[h][e] = 0.f;
+          }
         }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xp[pp][e] = make_float2(xv[0][e], xv[1][e]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&xempty[xs]);
@@ -190,9 +234,13 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
           ok = false;
           fail_sh = 1;
         }
-        float acc[kDecGroup * 8];  // index gg*8 + i
+        // acc2[pp][i] = partial sums of rank row i for rows (2pp, 2pp+1); each
+        // is the in-order fma chain over the lane's 8 elements
+        float2 acc2[kDecGroup / 2][kShRows];
 #pragma unroll
-        for (int j = 0; j < kDecGroup * 8; ++j) acc[j] = 0.f;
+        for (int pp = 0; pp < kDecGroup / 2; ++pp)
+#pragma unroll
+          for (int i = 0; i < kShRows; ++i) acc2[pp][i] = make_float2(0.f, 0.f);
         if (ok && has_k) {
           const uint16_t* st = ring + (size_t)s * kShRows * kDecKChunk + kk;
 #pragma unroll
@@ -201,12 +249,22 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
               float av[8];
               unpack8(*reinterpret_cast<const uint4*>(st + (size_t)i * kDecKChunk), av);
 #pragma unroll
-              for (int gg = 0; gg < kDecGroup; ++gg)
+              for (int e = 0; e < 8; ++e) {
+                const float2 a2 = make_float2(av[e], av[e]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[gg * 8 + i] = fmaf(av[e], xv[gg][e], acc[gg * 8 + i]);
+                for (int pp = 0; pp < kDecGroup / 2; ++pp) acc2[pp][i] = ffma2(a2, xp[pp][e], acc2[pp][i]);
+              }
             }
           }
         }
+        float acc[kDecGroup * 8];  // index gg*8 + i
+#pragma unroll
+        for (int pp = 0; pp < kDecGroup / 2; ++pp)
+#pragma unroll
+          for (int i = 0; i < kShRows; ++i) {
+            acc[(2 * pp) * 8 + i] = acc2[pp][i].x;
+            acc[(2 * pp + 1) * 8 + i] = acc2[pp][i].y;
+          }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         rs_step<32>(acc, lane, 16);
@@ -243,9 +301,11 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
   __shared__ __align__(8) uint64_t full_bar[kExStages], empty_bar[kExStages];
   __shared__ int fail_sh;
 
-  if (*p.status != 0) return;
+  pdl_wait();  // the previous kernel's results are visible from here on
+  const int status = *p.status, n_groups = p.counts[2];  // both loads in flight together
+  if (status != 0) return;
   const int total_nc = p.nc_base[p.L];
-  const int n_items = p.counts[2] * total_nc;
+  const int n_items = n_groups * total_nc;
   if ((int)blockIdx.x >= n_items) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -266,15 +326,13 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int w = item / total_nc, q = item - w * total_nc;
-        int l = 0;
-        while (l + 1 < p.L && q >= p.nc_base[l + 1]) ++l;
-        const int n0 = (q - p.nc_base[l]) * kDecNChunk;
+        int l, n0, dout, off;
+        pick_lane(p, q, l, n0, dout, off);
         const int k = p.work[w].x;
         const int r = p.rank_tab[k * p.L + l];
         if (r <= 0) continue;
-        const int dout = p.d_out[l];
         const int ncols = min(kDecNChunk, dout - n0);
-        const uint16_t* Bb = p.Bt[l] + (size_t)k * p.R16 * dout + n0;
+        const uint16_t* Bb = lane_param(p.Bt, l) + (size_t)k * p.R16 * dout + n0;
         for (int rb = 0; rb < r; rb += kExRows, ++fill) {
           const int s = fill % kExStages;
           if (fill >= kExStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kExStages) - 1) & 1, &fail_sh)) {
@@ -296,14 +354,12 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
     bool ok = true;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const int w = item / total_nc, q = item - w * total_nc;
-      int l = 0;
-      while (l + 1 < p.L && q >= p.nc_base[l + 1]) ++l;
-      const int n0 = (q - p.nc_base[l]) * kDecNChunk;
+      int l, n0, dout, off;
+      pick_lane(p, q, l, n0, dout, off);
       const int4 g = p.work[w];
       const int k = g.x, p0 = g.y, nrows = g.z - g.y;
       const int r = p.rank_tab[k * p.L + l];
       if (r <= 0) continue;
-      const int dout = p.d_out[l];
       named_bar_sync(1, kExWarps * 32);  // us of the previous item are no longer read
       for (int idx = tid; idx < r * kDecGroup; idx += kExWarps * 32) {
         const int i = idx >> 3, gg = idx & 7;
@@ -311,7 +367,15 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
         if (gg < nrows) {
           const float* u = p.u_dec + ((size_t)(p0 + gg) * p.L + l) * p.R16 + i;
           s = u[0];
-          for (int c = 1; c < p.C; ++c) s += u[c * cstride];
+          int c = 1;
+          for (; c + 8 <= p.C; c += 8) {  // eight loads in flight, added in chunk order
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = u[(size_t)(c + j) * cstride];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += v[j];
+          }
+          for (; c < p.C; ++c) s += u[(size_t)c * cstride];
         }
         us[i][gg] = s;
       }
@@ -319,15 +383,15 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
       const int o = n0 + kExCols * tid;
       const bool has = o < dout;
       float4 yv[kDecGroup];
-      float* const ycol = p.y + p.off[l] + o;
+      float* const ycol = p.y + off + o;
 #pragma unroll
       for (int gg = 0; gg < kDecGroup; ++gg)
         if (has && gg < nrows) yv[gg] = *reinterpret_cast<const float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy);
-      float acc[kDecGroup][kExCols];
+      float2 acc[kDecGroup][kExCols / 2];  // columns (2c, 2c+1) of row gg
 #pragma unroll
       for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
-        for (int e = 0; e < kExCols; ++e) acc[gg][e] = 0.f;
+        for (int e = 0; e < kExCols / 2; ++e) acc[gg][e] = make_float2(0.f, 0.f);
       const int nrb = (r + kExRows - 1) / kExRows;
       for (int rb = 0; rb < nrb; ++rb, ++use) {
         const int s = use % kExStages;
@@ -342,14 +406,17 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
             const int ri = rb * kExRows + i;
             if (ri < r) {
               const uint2 q2 = *reinterpret_cast<const uint2*>(st + (size_t)i * kDecNChunk);
-              const float bv[kExCols] = {bf16lo(q2.x), bf16hi(q2.x), bf16lo(q2.y), bf16hi(q2.y)};
+              const float2 b01 = make_float2(bf16lo(q2.x), bf16hi(q2.x));
+              const float2 b23 = make_float2(bf16lo(q2.y), bf16hi(q2.y));
               const float4 u0 = *reinterpret_cast<const float4*>(&us[ri][0]);
               const float4 u1 = *reinterpret_cast<const float4*>(&us[ri][4]);
               const float ug[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-              for (int gg = 0; gg < kDecGroup; ++gg)
-#pragma unroll
-                for (int e = 0; e < kExCols; ++e) acc[gg][e] = fmaf(bv[e], ug[gg], acc[gg][e]);
+              for (int gg = 0; gg < kDecGroup; ++gg) {
+                const float2 u2 = make_float2(ug[gg], ug[gg]);
+                acc[gg][0] = ffma2(b01, u2, acc[gg][0]);
+                acc[gg][1] = ffma2(b23, u2, acc[gg][1]);
+              }
             }
           }
         }
@@ -362,10 +429,10 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
       for (int gg = 0; gg < kDecGroup; ++gg) {
         if (gg < nrows) {
           float4 a = yv[gg];
-          a.x = fmaf(sc, acc[gg][0], a.x);
-          a.y = fmaf(sc, acc[gg][1], a.y);
-          a.z = fmaf(sc, acc[gg][2], a.z);
-          a.w = fmaf(sc, acc[gg][3], a.w);
+          a.x = fmaf(sc, acc[gg][0].x, a.x);
+          a.y = fmaf(sc, acc[gg][0].y, a.y);
+          a.z = fmaf(sc, acc[gg][1].x, a.z);
+          a.w = fmaf(sc, acc[gg][1].y, a.w);
           *reinterpret_cast<float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy) = a;
         }
       }
@@ -420,9 +487,9 @@ int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uin
   if (grid <= 0) return LORA_OK;
   const int smem = (int)(kShRingBytes + kShRedBytes + kShXBytes);
   if (!set_smem_limit(reinterpret_cast<const void*>(dec_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
-  dec_shrink_kernel<<<grid, kShThreads, smem, st>>>(p);
+  const cudaError_t e = launch_pdl(dec_shrink_kernel, dim3(grid), dim3(kShThreads), smem, st, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cuda_status(cudaGetLastError(), "dec_shrink_kernel launch");
+  return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "dec_shrink_kernel launch");
 }
 
 int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {
@@ -435,9 +502,9 @@ int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y,
   if (grid <= 0) return LORA_OK;
   const int smem = (int)kExRingBytes;
   if (!set_smem_limit(reinterpret_cast<const void*>(dec_expand_kernel), pool->device, smem)) return LORA_ERR_CUDA;
-  dec_expand_kernel<<<grid, kExThreads, smem, st>>>(p);
+  const cudaError_t e = launch_pdl(dec_expand_kernel, dim3(grid), dim3(kExThreads), smem, st, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cuda_status(cudaGetLastError(), "dec_expand_kernel launch");
+  return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "dec_expand_kernel launch");
 }
 
 }  // namespace lora

@@ -9,6 +9,15 @@
 
 namespace lora {
 
+// Programmatic dependent launch.  Every hot kernel is launched allowing it to
+// be scheduled before the kernel ahead of it on the stream has finished, and
+// waits, before its first global memory access, until that grid has finished
+// and its writes are visible.  Only the segment builder (one CTA) lets the
+// kernels after it launch at its start; a tensor expand launched that early
+// would hold whole SMs idle while the shrink drains, which measured slower.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Bounded waits give up after this many nanoseconds of %globaltimer and
 // report LORA_ERR_TIMEOUT through the status word.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -31,6 +40,19 @@ __device__ __forceinline__ void set_error(int32_t* status, int32_t code) {
 // Two bf16 values packed in a 32-bit word -> two floats (exact widening).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two independent fp32 fused multiply-adds in one instruction (packed f32x2,
+// round to nearest): (a.x * b.x + c.x, a.y * b.y + c.y), each exactly fmaf.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
 
 __device__ __forceinline__ void unpack8(const uint4& q, float (&f)[8]) {
   f[0] = bf16lo(q.x); f[1] = bf16hi(q.x);

@@ -104,6 +104,24 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
                      cudaStream_t st);
 int launch_repack(lora_pool* pool, int slot, int lane, int rank, float scale, const uint16_t* A,
                   const uint16_t* B, cudaStream_t st);
+// Launch `kernel` allowing programmatic dependent launch on `st` (the kernel
+// itself waits for its predecessor's results with griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
                       cudaStream_t st);
 int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy,

@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   __shared__ int scan_sums[3][33];
   __shared__ long long warp_len[kSegThreads / 32];
   __shared__ int warp_bad[kSegThreads / 32];
+  pdl_launch_next();  // the apply kernels may be scheduled now; they wait for this grid
+  pdl_wait();         // the previous kernel's results are visible from here on
 
   const int N = p.N, S = p.S, T = p.T;
   int* s_len = smem_dyn;           // [S] q_len
@@ -362,9 +364,9 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
   const size_t sm = sizeof(int) * seg_smem_ints(seg->N, S);
   if (sm > 48 * 1024 && !set_smem_limit(reinterpret_cast<const void*>(seg_build_kernel), seg->device, (int)sm))
     return LORA_ERR_CUDA;
-  seg_build_kernel<<<1, kSegThreads, sm, st>>>(p);
+  const cudaError_t e = launch_pdl(seg_build_kernel, dim3(1), dim3(kSegThreads), sm, st, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cuda_status(cudaGetLastError(), "seg_build_kernel launch");
+  return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "seg_build_kernel launch");
 }
 
 }  // namespace lora

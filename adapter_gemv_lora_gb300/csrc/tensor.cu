@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int fail_sh, last_sh;
 
+  pdl_wait();  // the previous kernel's results are visible from here on
   // A timeout is the only status a kernel of this step can raise while this
   // one runs; every other error is set before the launch and seen by all CTAs
   // alike, which keeps the per-tile arrival counts consistent.
@@ -382,6 +383,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int fail_sh;
 
+  pdl_wait();  // the previous kernel's results are visible from here on
   if (*p.status != 0) return;
   const int item = blockIdx.x;
   const int tile = item / p.total_ng;
@@ -659,9 +661,9 @@ int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint
   p.tmem_cols = cols;
   const int smem = p.ring_bytes + 1024;
   if (!set_smem_limit(reinterpret_cast<const void*>(tc_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
-  tc_shrink_kernel<<<grid, kTcThreads, smem, st>>>(tm_x128, tm_x32, pool->tm_a, p);
+  const cudaError_t e = launch_pdl(tc_shrink_kernel, dim3(grid), dim3(kTcThreads), smem, st, tm_x128, tm_x32, pool->tm_a, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cuda_status(cudaGetLastError(), "tc_shrink_kernel launch");
+  return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "tc_shrink_kernel launch");
 }
 
 int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {
@@ -687,9 +689,9 @@ int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, 
   p.R16 = pool->R16;
   const int smem = 2 * kHalfBytes + 4 * kTcTile * pool->R16 * 2 + 1024;  // staging + 2 B stages + U hi/lo
   if (!set_smem_limit(reinterpret_cast<const void*>(tc_expand_kernel), pool->device, smem)) return LORA_ERR_CUDA;
-  tc_expand_kernel<<<(unsigned)grid, kExpThreads, smem, st>>>(pool->tm_bk, p);
+  const cudaError_t e = launch_pdl(tc_expand_kernel, dim3((unsigned)grid), dim3(kExpThreads), smem, st, pool->tm_bk, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cuda_status(cudaGetLastError(), "tc_expand_kernel launch");
+  return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "tc_expand_kernel launch");
 }
 
 }  // namespace lora

@@ -60,6 +60,7 @@ struct DecParams {
   const uint16_t* A[LORA_MAX_LANES];
   const uint16_t* Bt[LORA_MAX_LANES];
   float* u_dec;
+  int32_t* sched;  // [2] the shrink's next-item and finished-CTA counters
   const uint16_t* x;
   int64_t ldx;
   float* y;
@@ -98,6 +99,22 @@ __device__ __forceinline__ void pick_lane(const DecParams& p, int q, int& l, int
   }
 }
 
+// Work items are handed out dynamically: every CTA starts with item
+// blockIdx.x and then takes tickets gridDim.x, gridDim.x + 1, ... from a
+// counter (item costs differ with the rank of their slot, so a fixed
+// round-robin split leaves some CTAs with several times the work of others).
+// The CTA that finishes last resets the counters to zero for the next launch;
+// which CTA runs an item never changes its result.
+__device__ __forceinline__ int next_item(int32_t* ctr) { return (int)gridDim.x + atomicAdd(ctr, 1); }
+
+__device__ __forceinline__ void finish_items(int32_t* ctr, int participants) {
+  __threadfence();  // this CTA's last ticket is taken before it counts itself out
+  if (atomicAdd(ctr + 1, 1) == participants - 1) {
+    ctr[0] = 0;
+    ctr[1] = 0;
+  }
+}
+
 // One step of a butterfly reduce-scatter: lanes exchange half of their values
 // with lane ^ o and keep the sum of the half selected by bit o of their id.
 template <int HALF>
@@ -117,11 +134,14 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
   float* red = reinterpret_cast<float*>(smem + kShRingBytes);  // [warp][rank block][64]
   uint16_t* xbuf = reinterpret_cast<uint16_t*>(smem + kShRingBytes + kShRedBytes);  // [2][row][kDecKChunk]
   __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages], xfull[2], xempty[2];
+  __shared__ int4 sitem[2];  // {rank | rows << 8 | lane << 16 (0 = no more items), K chunk, first perm row, -}
   __shared__ int fail_sh;
 
   pdl_wait();  // the previous kernel's results are visible from here on
   const int status = *p.status, n_groups = p.counts[2];  // both loads in flight together
-  if (status != 0) return;
+  // a timeout is the only status another kernel can raise while this one runs;
+  // every CTA of the grid takes part in the item counting whatever it reads
+  if (status != 0 && status != LORA_ERR_TIMEOUT) return;
   const int per_group = p.L * p.C;
   const int n_items = n_groups * per_group;
   if ((int)blockIdx.x >= n_items) return;
@@ -141,37 +161,46 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
   __syncthreads();
 
   if (warp == kShWarps) {
-    // ---------------- producer: the group's x rows of this chunk, then the slot's A rows
+    // ---------------- producer: per item, the group's x rows of its K chunk, then the slot's A rows
     if (lane == 0) {
       uint32_t fill = 0, xj = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int w = item / per_group, rem = item - w * per_group;
-        const int l = rem / p.C, c = rem - l * p.C;
-        const int k = p.work[w].x;
-        const int r = p.rank_tab[k * p.L + l];
-        if (r <= 0) continue;
-        const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
-        {
-          const int4 g = p.work[w];
-          const int nrows = g.z - g.y, xs = xj & 1;
-          if (xj >= 2 && !mbar_wait_or_fail(&xempty[xs], ((xj >> 1) - 1) & 1, &fail_sh)) {
-            ok = false;
-            fail_sh = 1;
-            break;
-          }
-          int row[kDecGroup];  // all row indexes first: the copies below are ordered memory operations
-#pragma unroll
-          for (int gg = 0; gg < kDecGroup; ++gg) row[gg] = gg < nrows ? p.perm[g.y + gg] : 0;
-          mbar_expect_tx(&xfull[xs], (uint32_t)(nrows * klen * 2));
-#pragma unroll
-          for (int gg = 0; gg < kDecGroup; ++gg)
-            if (gg < nrows)
-              bulk_load(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk, p.x + (size_t)row[gg] * p.ldx + k0,
-                        (uint32_t)(klen * 2), &xfull[xs]);
-          ++xj;
+      int item = blockIdx.x;
+      for (;;) {
+        int r = 0, l = 0, c = 0;
+        int4 g = make_int4(0, 0, 0, 0);
+        for (; item < n_items; item = next_item(p.sched)) {  // items of a rank-0 lane do nothing
+          const int w = item / per_group, rem = item - w * per_group;
+          l = rem / p.C;
+          c = rem - l * p.C;
+          g = p.work[w];
+          r = p.rank_tab[g.x * p.L + l];
+          if (r > 0) break;
         }
-        const uint16_t* Ab = lane_param(p.A, l) + (size_t)k * p.R16 * p.d_in + k0;
+        const int xs = xj & 1;
+        if (xj >= 2 && !mbar_wait_or_fail(&xempty[xs], ((xj >> 1) - 1) & 1, &fail_sh)) {
+          fail_sh = 1;
+          break;
+        }
+        if (item >= n_items) {  // no more items: an empty buffer tells the compute warps
+          sitem[xs] = make_int4(0, 0, 0, 0);
+          mbar_arrive(&xfull[xs]);
+          break;
+        }
+        const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
+        const int nrows = g.z - g.y;
+        sitem[xs] = make_int4(r | (nrows << 8) | (l << 16), c, g.y, 0);
+        int row[kDecGroup];  // all row indexes first: the copies below are ordered memory operations
+#pragma unroll
+        for (int gg = 0; gg < kDecGroup; ++gg) row[gg] = gg < nrows ? p.perm[g.y + gg] : 0;
+        mbar_expect_tx(&xfull[xs], (uint32_t)(nrows * klen * 2));
+#pragma unroll
+        for (int gg = 0; gg < kDecGroup; ++gg)
+          if (gg < nrows)
+            bulk_load(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk, p.x + (size_t)row[gg] * p.ldx + k0,
+                      (uint32_t)(klen * 2), &xfull[xs]);
+        ++xj;
+        const uint16_t* Ab = lane_param(p.A, l) + (size_t)g.x * p.R16 * p.d_in + k0;
+        bool ok = true;
         for (int rb = 0; rb < r; rb += kShRows, ++fill) {
           const int s = fill % kShStages;
           if (fill >= kShStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kShStages) - 1) & 1, &fail_sh)) {
@@ -185,27 +214,27 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
             bulk_load(ring + ((size_t)s * kShRows + i) * kDecKChunk, Ab + (size_t)(rb + i) * p.d_in,
                       (uint32_t)(klen * 2), &full_bar[s]);
         }
+        if (!ok) break;
+        item = next_item(p.sched);
       }
+      finish_items(p.sched, min((int)gridDim.x, n_items));
     }
   } else {
-    // ---------------- compute warps
+    // ---------------- compute warps: the items the producer hands over with their x rows
     uint32_t use = 0, xj = 0;
     bool ok = true;
     const int kk = warp * 256 + lane * 8;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const int w = item / per_group, rem = item - w * per_group;
-      const int l = rem / p.C, c = rem - l * p.C;
-      const int4 g = p.work[w];
-      const int k = g.x, p0 = g.y, nrows = g.z - g.y;
-      const int r = p.rank_tab[k * p.L + l];
-      if (r <= 0) continue;
+    for (;;) {
+      const int xs = xj & 1;
+      if (!ok || !mbar_wait_or_fail(&xfull[xs], (xj >> 1) & 1, &fail_sh)) {
+        fail_sh = 1;
+        break;
+      }
+      const int4 it = sitem[xs];
+      const int r = it.x & 0xff, nrows = (it.x >> 8) & 0xff, l = it.x >> 16, c = it.y, p0 = it.z;
+      if (r <= 0) break;  // no more items
       const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
       const bool has_k = kk < klen;
-      const int xs = xj & 1;
-      if (ok && !mbar_wait_or_fail(&xfull[xs], (xj >> 1) & 1, &fail_sh)) {
-        ok = false;
-        fail_sh = 1;
-      }
       // x of rows 2p and 2p+1 side by side, for the packed fma
       float2 xp[kDecGroup / 2][8];
 #pragma unroll
@@ -457,6 +486,7 @@ DecParams make_params(const lora_pool* pool, const lora_segments* seg) {
     p.off[l] = pool->off[l];
   }
   p.u_dec = pool->u_dec;
+  p.sched = pool->dec_sched;
   p.L = pool->L;
   p.R16 = pool->R16;
   p.d_in = pool->d_in;

@@ -65,6 +65,7 @@ struct lora_pool {
   uint16_t* u_fmt = nullptr;        // [tc_tile_cap][L][2][128*R16] per tensor tile: U as bf16 hi then lo,
                                     // K-major core-matrix layout of the tile's own rank, ready for the expand
   int32_t* tile_cnt = nullptr;      // [tc_tile_cap] K-range CTAs of a tile that finished (0 between calls)
+  int32_t* dec_sched = nullptr;     // [4] decode shrink's item and finished-CTA counters (0 between calls)
   std::vector<int> h_rank;          // host mirror of rank_tab
   lora::TmapSized tm_a;             // A, 3-D {d_in, R16, N}, box {64, 16<<s, 1}, 128-byte swizzle
   lora::TmapSized tm_bk;            // Bk, 3-D {16, d_out, R16/16*N}, box {16, 128, 1<<s}, 32-byte swizzle

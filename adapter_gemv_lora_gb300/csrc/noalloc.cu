@@ -25,11 +25,12 @@
 namespace {
 
 constexpr size_t kScratchFloats = (size_t)LORA_NOALLOC_SCRATCH_BYTES / sizeof(float);
-// Per-tile arrival counters of the tensor shrink sit at the start of the
-// array, where they keep their between-calls value of zero (the array is
-// zero when the library loads, and each call leaves the counts it used at
-// zero).
-constexpr size_t kCounterWords = 16384;
+// The tensor shrink's per-tile arrival counters and the decode kernels' item
+// counters sit at the start of the array, where they keep their between-calls
+// value of zero (the array is zero when the library loads, and each call
+// leaves the counts it used at zero).
+constexpr size_t kTileCounters = 16384;
+constexpr size_t kCounterWords = kTileCounters + 64;  // + the decode kernels' item counters
 
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
@@ -73,7 +74,7 @@ extern "C" int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lor
   const size_t tc_floats = (size_t)lora::kTcKSplit * tiles * per_row * lora::kTcTile;
   const size_t fmt_floats = tiles * per_row * lora::kTcTile;  // 2 bf16 halves = 1 float per element
   const size_t need = kCounterWords + dec_floats + tc_floats + fmt_floats;
-  if (tiles > kCounterWords || need > kScratchFloats) return LORA_ERR_SHAPE;
+  if (tiles > kTileCounters || need > kScratchFloats) return LORA_ERR_SHAPE;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
@@ -108,6 +109,7 @@ extern "C" int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lor
   view.tm_a = pool->tm_a;
   view.tm_bk = pool->tm_bk;
   view.tile_cnt = reinterpret_cast<int32_t*>(scratch);
+  view.dec_sched = reinterpret_cast<int32_t*>(scratch) + kTileCounters;
   view.u_dec = scratch + kCounterWords;
   view.u_tc = view.u_dec + dec_floats;
   view.u_fmt = reinterpret_cast<uint16_t*>(view.u_tc + tc_floats);

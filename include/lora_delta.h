@@ -210,7 +210,7 @@ int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void
  *   - The rank-space intermediate lives in a fixed array compiled into the
  *     library, of LORA_NOALLOC_SCRATCH_BYTES; every GPU that loads the
  *     library holds it until the process exits.  A step needs, in floats,
- *     16384 (per-tile counters) + C * T * num_lanes * R16 (decode partial
+ *     16448 (counters) + C * T * num_lanes * R16 (decode partial
  *     sums, C = ceil(d_in / 1024)) + 3 * (T / 64 + 1) * num_lanes * R16 * 128
  *     (tensor-path partial sums and U tiles); one that needs more returns
  *     LORA_ERR_SHAPE before anything is enqueued.

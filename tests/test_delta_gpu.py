@@ -48,6 +48,35 @@ def test_mixed_small_full_oracle(oracle_mod):
     _oracle_check(oracle_mod, wl, wl.projections[0], what="mixed")
 
 
+def test_pool_reused_across_steps(oracle_mod):
+    # one pool, several steps with different batches: the per-tile and
+    # work-item counters the kernels keep in the pool's scratch must be back
+    # at zero after every step, so each step matches the oracle and a repeated
+    # step repeats its bits
+    from adapter_gemv_lora_gb300 import lora_delta as LD  # noqa: F401
+    base = _mixed_workload(seed=11)
+    proj = base.projections[0]
+    pool = TL.build_pool(proj, base.T)
+    rng = np.random.default_rng(5)
+    first = None
+    for step in range(4):
+        lens = rng.choice([1, 1, 2, 64, 70, 129, 300], size=int(rng.integers(3, 10)))
+        lens = lens[np.cumsum(lens) <= base.T]  # the rows must fit the workload's x and y0
+        ids = rng.integers(0, base.num_slots, size=len(lens))
+        T = int(lens.sum())
+        x, y0 = proj.x[:T], proj.y0[:T]
+        slot = np.repeat(ids, lens)
+        y = TL.run_gpu(proj, ids, lens, x=x, y0=y0, pool=pool)
+        _, dref = oracle_mod.delta(proj, slot, rows=np.arange(T), x=x, y0=y0)
+        TL.assert_delta_close(y, y0, dref, f"step {step}")
+        if first is None:
+            first = (ids, lens, y)
+    ids, lens, y_first = first
+    T = int(lens.sum())
+    y_again = TL.run_gpu(proj, ids, lens, x=proj.x[:T], y0=proj.y0[:T], pool=pool)
+    assert np.array_equal(y_again.view(np.uint32), y_first.view(np.uint32))
+
+
 @pytest.mark.parametrize("d_in", [64, 192, 1088])
 def test_k_block_counts(oracle_mod, d_in):
     # d_in of 1, 3 and 17 blocks of 64: the tensor shrink's two K ranges are

@@ -124,6 +124,14 @@ SideStream* side_stream() {
   return &s;
 }
 
+}  // namespace
+
+// Creates the current device's side stream and events if they do not exist
+// yet (outside any stream capture, from pool creation).
+bool lora::ensure_side_stream() { return side_stream() != nullptr; }
+
+namespace {
+
 bool any_loaded(const lora_pool* pool) {
   for (int v : pool->h_rank)
     if (v > 0) return true;

@@ -100,6 +100,9 @@ bool set_smem_limit(const void* kernel, int device, int bytes);
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* addr, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
 
+// The apply's side stream for the current device, created on first use.
+bool ensure_side_stream();
+
 // Launchers (return a LORA_* status).
 int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens, int S, int T,
                      cudaStream_t st);

@@ -137,6 +137,7 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   PoolLayout P;
   if (!pool_layout(num_slots, max_rank, d_in, num_lanes, lane_d_out, max_tokens, &P)) return LORA_ERR_SHAPE;
   if (bytes < P.total) return LORA_ERR_SHAPE;
+  ensure_side_stream();  // now, not inside a caller's stream capture (the apply works without it)
   lora_pool* p = new lora_pool();
   if (cudaGetDevice(&p->device) != cudaSuccess) {
     delete p;

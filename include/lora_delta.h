@@ -97,7 +97,9 @@ size_t lora_pool_bytes(int num_slots, int max_rank, int d_in, int num_lanes,
 /* Create a pool descriptor over caller memory dev_mem (>= lora_pool_bytes,
  * 256-byte aligned).  Enqueues a zero fill of dev_mem on `stream`, so every
  * slot starts unloaded (rank 0).  The descriptor records the current CUDA
- * device.  Errors: LORA_ERR_ARG, LORA_ERR_SHAPE, LORA_ERR_CUDA. */
+ * device; the first pool of a device also creates the library's side stream
+ * and events for that device (see lora_apply_shrink_expand).  Errors:
+ * LORA_ERR_ARG, LORA_ERR_SHAPE, LORA_ERR_CUDA. */
 int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots, int max_rank,
                      int d_in, int num_lanes, const int* lane_d_out /* host */, int max_tokens,
                      lora_stream_t stream);

@@ -77,6 +77,45 @@ def test_pool_reused_across_steps(oracle_mod):
     assert np.array_equal(y_again.view(np.uint32), y_first.view(np.uint32))
 
 
+def test_graph_capture_matches_eager():
+    # build + apply captured in a CUDA graph (the apply forks its decode
+    # kernels onto the library's side stream and joins them back) replays to
+    # the same bits as the eager calls
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    wl = _mixed_workload(seed=3)
+    proj = wl.projections[0]
+    pool = TL.build_pool(proj, wl.T)
+    seg = LD.LoraSegments(wl.S, wl.T, wl.num_slots, device="cuda")
+    ids = torch.tensor(wl.adapter_ids, dtype=torch.int32, device="cuda")
+    lens = torch.tensor(wl.q_seq_lens, dtype=torch.int32, device="cuda")
+    x = TL.to_dev_u16(proj.x, "cuda")
+    y0 = torch.from_numpy(proj.y0).cuda()
+    y = y0.clone()
+
+    def step():
+        seg.build(ids, lens, num_tokens=wl.T)
+        LD.apply(pool, seg, x, y)
+
+    step()
+    torch.cuda.synchronize()
+    y_eager = y.clone()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        y.copy_(y0)
+        with torch.cuda.graph(g):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        y.copy_(y0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int32), y_eager.view(torch.int32))
+    assert seg.status() == 0
+
+
 @pytest.mark.parametrize("d_in", [64, 192, 1088])
 def test_k_block_counts(oracle_mod, d_in):
     # d_in of 1, 3 and 17 blocks of 64: the tensor shrink's two K ranges are

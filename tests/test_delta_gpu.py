@@ -116,6 +116,30 @@ def test_graph_capture_matches_eager():
     assert seg.status() == 0
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes_full_oracle(oracle_mod, seed):
+    # random d_in, lane count and widths, rank bounds (including ranks that are
+    # not multiples of 16 and zero lanes), slot counts and length mixes around
+    # the path threshold and the tile size; every row against the oracle
+    rng = np.random.default_rng(1000 + seed)
+    d_in = int(rng.choice([64, 128, 640, 1024, 2112, 4096]))
+    L = int(rng.integers(1, 5))
+    lanes = [int(64 * rng.integers(1, 17)) for _ in range(L)]
+    max_rank = int(rng.choice([r for r in (1, 7, 16, 33, 64, 100, 128) if L * ((r + 15) // 16 * 16) <= 256]))
+    N = int(rng.integers(2, 13))
+    S = int(rng.integers(1, 40))
+    lens = rng.choice([0, 1, 1, 1, 2, 7, 63, 64, 65, 127, 128, 129, 300], size=S)
+    while lens.sum() == 0:
+        lens = rng.choice([1, 64, 129], size=S)
+    ids = rng.integers(0, N, size=S)
+    rank = rng.integers(0, max_rank + 1, size=(N, L)).astype(np.int32)
+    rank[0] = 0
+    rank[rng.random((N, L)) < 0.15] = 0
+    wl = W.custom_workload(lens, ids, d_in=d_in, lane_d_out=lanes, num_slots=N, max_rank=max_rank, rank=rank,
+                           seed=seed)
+    _oracle_check(oracle_mod, wl, wl.projections[0], what=f"seed {seed}: d_in {d_in} lanes {lanes} R {max_rank}")
+
+
 @pytest.mark.parametrize("d_in", [64, 192, 1088])
 def test_k_block_counts(oracle_mod, d_in):
     # d_in of 1, 3 and 17 blocks of 64: the tensor shrink's two K ranges are

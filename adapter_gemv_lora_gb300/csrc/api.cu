@@ -145,6 +145,10 @@ int check_apply(const lora_pool* pool, const lora_segments* seg, const void* x, 
   if (ldx < pool->d_in || ldy < pool->D || (ldx % 8) || (ldy % 4)) return LORA_ERR_ARG;
   if (seg->N != pool->N) return LORA_ERR_SHAPE;
   if (seg->T > pool->max_tokens) return LORA_ERR_SHAPE;
+  // the kernels run on the current device: the pool and the segments must live there
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  if (dev != pool->device || dev != seg->device) return LORA_ERR_ARG;
   return LORA_OK;
 }
 

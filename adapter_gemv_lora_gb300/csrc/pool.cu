@@ -213,6 +213,9 @@ int lora_pool_load(lora_pool* pool, int slot, int lane, int rank, float scale, c
   if (rank < 0 || rank > pool->R) return LORA_ERR_RANK;
   if (rank > 0 && (!A || !B)) return LORA_ERR_ARG;
   if (rank > 0 && (reinterpret_cast<uintptr_t>(A) & 1 || reinterpret_cast<uintptr_t>(B) & 1)) return LORA_ERR_ARG;
+  int dev = -1;  // the repack runs on the current device, where the pool must live
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  if (dev != pool->device) return LORA_ERR_ARG;
   const int st = launch_repack(pool, slot, lane, rank, rank > 0 ? scale : 0.0f,
                                static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B),
                                reinterpret_cast<cudaStream_t>(stream));

@@ -457,6 +457,9 @@ int lora_build_segments(lora_segments* seg, const int32_t* adapter_ids, const in
     return cudaMemsetAsync(seg->status, 0, 4, st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
   }
   if (!adapter_ids || !q_seq_lens) return LORA_ERR_ARG;
+  int dev = -1;  // the builder runs on the current device, where the workspace must live
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  if (dev != seg->device) return LORA_ERR_ARG;
   seg->S = num_seqs;
   seg->T = num_tokens;
   return launch_seg_build(seg, adapter_ids, q_seq_lens, num_seqs, num_tokens, st);

@@ -51,7 +51,8 @@ typedef struct CUstream_st* lora_stream_t; /* identical to cudaStream_t */
 /* Status codes. */
 enum {
   LORA_OK = 0,
-  LORA_ERR_ARG = -1,     /* null pointer, misaligned pointer, bad leading dimension   */
+  LORA_ERR_ARG = -1,     /* null pointer, misaligned pointer, bad leading dimension, or
+                            a call made while another device than the object's is current */
   LORA_ERR_SHAPE = -2,   /* unsupported or inconsistent sizes                          */
   LORA_ERR_SLOT = -3,    /* a slot id outside [0, num_slots) (host or device detected) */
   LORA_ERR_RANK = -4,    /* rank outside [0, max_rank]                                 */

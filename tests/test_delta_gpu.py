@@ -140,6 +140,81 @@ def test_random_shapes_full_oracle(oracle_mod, seed):
     _oracle_check(oracle_mod, wl, wl.projections[0], what=f"seed {seed}: d_in {d_in} lanes {lanes} R {max_rank}")
 
 
+def test_one_graph_serves_any_adapter_mixture(oracle_mod):
+    # captured once for a (num_seqs, num_tokens) shape, the step replays for
+    # other adapter ids and other length splits of the same totals: the work
+    # lists live in device memory and the grids are sized by capacity
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    wl = _mixed_workload(seed=6)
+    proj = wl.projections[0]
+    pool = TL.build_pool(proj, wl.T)
+    seg = LD.LoraSegments(wl.S, wl.T, wl.num_slots, device="cuda")
+    ids = torch.tensor(wl.adapter_ids, dtype=torch.int32, device="cuda")
+    lens = torch.tensor(wl.q_seq_lens, dtype=torch.int32, device="cuda")
+    x = TL.to_dev_u16(proj.x, "cuda")
+    y0 = torch.from_numpy(proj.y0).cuda()
+    y = y0.clone()
+    g = torch.cuda.CUDAGraph()
+    s_ = torch.cuda.Stream()
+    s_.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_):
+        seg.build(ids, lens, num_tokens=wl.T)  # one eager step before capture
+        LD.apply(pool, seg, x, y)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            seg.build(ids, lens, num_tokens=wl.T)
+            LD.apply(pool, seg, x, y)
+    torch.cuda.current_stream().wait_stream(s_)
+    rng = np.random.default_rng(9)
+    for mix in range(3):
+        new_ids = rng.integers(0, wl.num_slots, size=wl.S).astype(np.int32)
+        cut = np.sort(rng.choice(np.arange(1, wl.T), size=wl.S - 1, replace=False))
+        new_lens = np.diff(np.concatenate([[0], cut, [wl.T]])).astype(np.int32)
+        ids.copy_(torch.from_numpy(new_ids))
+        lens.copy_(torch.from_numpy(new_lens))
+        y.copy_(y0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert seg.status() == 0
+        slot = np.repeat(new_ids, new_lens)
+        _, dref = oracle_mod.delta(proj, slot)
+        got = y.cpu().numpy()
+        TL.assert_delta_close(got, proj.y0, dref, f"mixture {mix}")
+        TL.assert_rows_untouched(got, proj.y0, np.nonzero(slot == 0)[0])
+
+
+@pytest.mark.parametrize("shards", [2, 4])
+def test_row_parallel_shards_sum_to_the_delta(oracle_mod, shards):
+    # row-parallel layers (o_proj, down) under tensor parallelism cut A by
+    # columns: rank p holds A[:, cols_p] and x[:, cols_p] and adds
+    # scale * B @ (A_p @ x_p) into its partial sum, which the base's reduction
+    # adds up.  Each shard is an ordinary pool of d_in / shards; summing the
+    # shards' deltas on the host gives the full delta
+    import torch
+    base = _mixed_workload(seed=8, lanes=(256,))
+    proj = base.projections[0]
+    d_in = proj.d_in
+    part = d_in // shards
+    total = np.zeros_like(proj.y0, dtype=np.float64)
+    for sh in range(shards):
+        cols = slice(sh * part, (sh + 1) * part)
+        wl_p = W.custom_workload(base.q_seq_lens, base.adapter_ids, d_in=part, lane_d_out=[256],
+                                 num_slots=base.num_slots, max_rank=32, rank=proj.rank, seed=0)
+        pp = wl_p.projections[0]
+        for k in range(1, base.num_slots):
+            if proj.rank[k, 0] > 0:
+                pp.A[k][0] = np.ascontiguousarray(proj.A[k][0][:, cols])
+                pp.B[k][0] = proj.B[k][0]
+        pp.scale[:] = proj.scale
+        zeros = np.zeros_like(proj.y0)
+        y = TL.run_gpu(pp, base.adapter_ids, base.q_seq_lens, x=np.ascontiguousarray(proj.x[:, cols]), y0=zeros)
+        total += y.astype(np.float64)
+    _, dref = oracle_mod.delta(proj, base.per_token_slot())
+    TL.assert_delta_close((proj.y0.astype(np.float64) + total).astype(np.float32), proj.y0, dref,
+                          f"{shards} row-parallel shards")
+
+
 @pytest.mark.parametrize("d_in", [64, 192, 1088])
 def test_k_block_counts(oracle_mod, d_in):
     # d_in of 1, 3 and 17 blocks of 64: the tensor shrink's two K ranges are

@@ -80,27 +80,8 @@ __device__ __forceinline__ V lane_param(const V (&a)[LORA_MAX_LANES], int l) {
   return v;
 }
 
-// Lane, first column, width and y offset of expand column chunk q, picked with
-// constant indexes (a parameter array indexed at run time would be copied to
-// local memory).
-__device__ __forceinline__ void pick_lane(const DecParams& p, int q, int& l, int& n0, int& dout, int& off) {
-  l = 0;
-  n0 = q * kDecNChunk;
-  dout = p.d_out[0];
-  off = p.off[0];
-#pragma unroll
-  for (int i = 1; i < LORA_MAX_LANES; ++i) {
-    if (i < p.L && q >= p.nc_base[i]) {
-      l = i;
-      n0 = (q - p.nc_base[i]) * kDecNChunk;
-      dout = p.d_out[i];
-      off = p.off[i];
-    }
-  }
-}
-
-// Work items are handed out dynamically: every CTA starts with item
-// blockIdx.x and then takes tickets gridDim.x, gridDim.x + 1, ... from a
+// Work items of the shrink are handed out dynamically: every CTA starts with
+// item blockIdx.x and then takes tickets gridDim.x, gridDim.x + 1, ... from a
 // counter (item costs differ with the rank of their slot, so a fixed
 // round-robin split leaves some CTAs with several times the work of others).
 // The CTA that finishes last resets the counters to zero for the next launch;
@@ -112,6 +93,51 @@ __device__ __forceinline__ void finish_items(int32_t* ctr, int participants) {
   if (atomicAdd(ctr + 1, 1) == participants - 1) {
     ctr[0] = 0;
     ctr[1] = 0;
+  }
+}
+
+// Expand items cover `ncb` consecutive 1024-column blocks of one lane, so the
+// group's u (the sum of the shrink's chunk partials) is formed once per ncb
+// blocks.  ncb is the largest of 1, 2, 4 that still leaves every CTA of the
+// grid at least two items; it depends on the step's real number of decode
+// groups, so every CTA computes the same value.  Results do not depend on it.
+struct ExGeom {
+  int ncb, total, base[LORA_MAX_LANES + 1];  // items per lane start at base[l]
+};
+
+__device__ __forceinline__ ExGeom ex_geom(const DecParams& p, int n_groups) {
+  ExGeom g;
+  g.ncb = 1;
+  for (int cand = 2; cand <= 4; cand *= 2) {
+    int per_group = 0;
+#pragma unroll
+    for (int l = 0; l < LORA_MAX_LANES; ++l)
+      if (l < p.L) per_group += (p.nc_base[l + 1] - p.nc_base[l] + cand - 1) / cand;
+    if ((long long)n_groups * per_group >= 2LL * gridDim.x) g.ncb = cand;
+  }
+  g.base[0] = 0;
+#pragma unroll
+  for (int l = 0; l < LORA_MAX_LANES; ++l)
+    g.base[l + 1] = g.base[l] + (l < p.L ? (p.nc_base[l + 1] - p.nc_base[l] + g.ncb - 1) / g.ncb : 0);
+  g.total = g.base[LORA_MAX_LANES];
+  return g;
+}
+
+// Lane, first column, width and y offset of expand item column range q.
+__device__ __forceinline__ void pick_item_lane(const DecParams& p, const ExGeom& g, int q, int& l, int& n0, int& dout,
+                                               int& off) {
+  l = 0;
+  n0 = q * g.ncb * kDecNChunk;
+  dout = p.d_out[0];
+  off = p.off[0];
+#pragma unroll
+  for (int i = 1; i < LORA_MAX_LANES; ++i) {
+    if (i < p.L && q >= g.base[i]) {
+      l = i;
+      n0 = (q - g.base[i]) * g.ncb * kDecNChunk;
+      dout = p.d_out[i];
+      off = p.off[i];
+    }
   }
 }
 
@@ -333,7 +359,8 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
   pdl_wait();  // the previous kernel's results are visible from here on
   const int status = *p.status, n_groups = p.counts[2];  // both loads in flight together
   if (status != 0) return;
-  const int total_nc = p.nc_base[p.L];
+  const ExGeom geom = ex_geom(p, n_groups);
+  const int total_nc = geom.total;
   const int n_items = n_groups * total_nc;
   if ((int)blockIdx.x >= n_items) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -356,24 +383,26 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int w = item / total_nc, q = item - w * total_nc;
         int l, n0, dout, off;
-        pick_lane(p, q, l, n0, dout, off);
+        pick_item_lane(p, geom, q, l, n0, dout, off);
         const int k = p.work[w].x;
         const int r = p.rank_tab[k * p.L + l];
         if (r <= 0) continue;
-        const int ncols = min(kDecNChunk, dout - n0);
-        const uint16_t* Bb = lane_param(p.Bt, l) + (size_t)k * p.R16 * dout + n0;
-        for (int rb = 0; rb < r; rb += kExRows, ++fill) {
-          const int s = fill % kExStages;
-          if (fill >= kExStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kExStages) - 1) & 1, &fail_sh)) {
-            ok = false;
-            fail_sh = 1;
-            break;
+        for (int nb = n0; nb < min(dout, n0 + geom.ncb * kDecNChunk) && ok; nb += kDecNChunk) {
+          const int ncols = min(kDecNChunk, dout - nb);
+          const uint16_t* Bb = lane_param(p.Bt, l) + (size_t)k * p.R16 * dout + nb;
+          for (int rb = 0; rb < r; rb += kExRows, ++fill) {
+            const int s = fill % kExStages;
+            if (fill >= kExStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kExStages) - 1) & 1, &fail_sh)) {
+              ok = false;
+              fail_sh = 1;
+              break;
+            }
+            const int rows = min(kExRows, r - rb);
+            mbar_expect_tx(&full_bar[s], (uint32_t)(rows * ncols * 2));
+            for (int i = 0; i < rows; ++i)
+              bulk_load(ring + ((size_t)s * kExRows + i) * kDecNChunk, Bb + (size_t)(rb + i) * dout,
+                        (uint32_t)(ncols * 2), &full_bar[s]);
           }
-          const int rows = min(kExRows, r - rb);
-          mbar_expect_tx(&full_bar[s], (uint32_t)(rows * ncols * 2));
-          for (int i = 0; i < rows; ++i)
-            bulk_load(ring + ((size_t)s * kExRows + i) * kDecNChunk, Bb + (size_t)(rb + i) * dout,
-                      (uint32_t)(ncols * 2), &full_bar[s]);
         }
       }
     }
@@ -384,7 +413,7 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const int w = item / total_nc, q = item - w * total_nc;
       int l, n0, dout, off;
-      pick_lane(p, q, l, n0, dout, off);
+      pick_item_lane(p, geom, q, l, n0, dout, off);
       const int4 g = p.work[w];
       const int k = g.x, p0 = g.y, nrows = g.z - g.y;
       const int r = p.rank_tab[k * p.L + l];
@@ -409,60 +438,62 @@ __global__ void __launch_bounds__(kExThreads, 2) dec_expand_kernel(DecParams p) 
         us[i][gg] = s;
       }
       named_bar_sync(1, kExWarps * 32);
-      const int o = n0 + kExCols * tid;
-      const bool has = o < dout;
-      float4 yv[kDecGroup];
-      float* const ycol = p.y + off + o;
+      const float sc = p.scale_tab[k * p.L + l];
+      for (int nb = n0; nb < min(dout, n0 + geom.ncb * kDecNChunk) && ok; nb += kDecNChunk) {
+        const int o = nb + kExCols * tid;
+        const bool has = o < dout;
+        float4 yv[kDecGroup];
+        float* const ycol = p.y + off + o;
 #pragma unroll
-      for (int gg = 0; gg < kDecGroup; ++gg)
-        if (has && gg < nrows) yv[gg] = *reinterpret_cast<const float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy);
-      float2 acc[kDecGroup][kExCols / 2];  // columns (2c, 2c+1) of row gg
+        for (int gg = 0; gg < kDecGroup; ++gg)
+          if (has && gg < nrows) yv[gg] = *reinterpret_cast<const float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy);
+        float2 acc[kDecGroup][kExCols / 2];  // columns (2c, 2c+1) of row gg
 #pragma unroll
-      for (int gg = 0; gg < kDecGroup; ++gg)
+        for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
-        for (int e = 0; e < kExCols / 2; ++e) acc[gg][e] = make_float2(0.f, 0.f);
-      const int nrb = (r + kExRows - 1) / kExRows;
-      for (int rb = 0; rb < nrb; ++rb, ++use) {
-        const int s = use % kExStages;
-        if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kExStages) & 1, &fail_sh)) {
-          ok = false;
-          fail_sh = 1;
-        }
-        if (ok && has) {
-          const uint16_t* st = ring + (size_t)s * kExRows * kDecNChunk + kExCols * tid;
+          for (int e = 0; e < kExCols / 2; ++e) acc[gg][e] = make_float2(0.f, 0.f);
+        const int nrb = (r + kExRows - 1) / kExRows;
+        for (int rb = 0; rb < nrb; ++rb, ++use) {
+          const int s = use % kExStages;
+          if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kExStages) & 1, &fail_sh)) {
+            ok = false;
+            fail_sh = 1;
+          }
+          if (ok && has) {
+            const uint16_t* st = ring + (size_t)s * kExRows * kDecNChunk + kExCols * tid;
 #pragma unroll 4
-          for (int i = 0; i < kExRows; ++i) {
-            const int ri = rb * kExRows + i;
-            if (ri < r) {
-              const uint2 q2 = *reinterpret_cast<const uint2*>(st + (size_t)i * kDecNChunk);
-              const float2 b01 = make_float2(bf16lo(q2.x), bf16hi(q2.x));
-              const float2 b23 = make_float2(bf16lo(q2.y), bf16hi(q2.y));
-              const float4 u0 = *reinterpret_cast<const float4*>(&us[ri][0]);
-              const float4 u1 = *reinterpret_cast<const float4*>(&us[ri][4]);
-              const float ug[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            for (int i = 0; i < kExRows; ++i) {
+              const int ri = rb * kExRows + i;
+              if (ri < r) {
+                const uint2 q2 = *reinterpret_cast<const uint2*>(st + (size_t)i * kDecNChunk);
+                const float2 b01 = make_float2(bf16lo(q2.x), bf16hi(q2.x));
+                const float2 b23 = make_float2(bf16lo(q2.y), bf16hi(q2.y));
+                const float4 u0 = *reinterpret_cast<const float4*>(&us[ri][0]);
+                const float4 u1 = *reinterpret_cast<const float4*>(&us[ri][4]);
+                const float ug[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-              for (int gg = 0; gg < kDecGroup; ++gg) {
-                const float2 u2 = make_float2(ug[gg], ug[gg]);
-                acc[gg][0] = ffma2(b01, u2, acc[gg][0]);
-                acc[gg][1] = ffma2(b23, u2, acc[gg][1]);
+                for (int gg = 0; gg < kDecGroup; ++gg) {
+                  const float2 u2 = make_float2(ug[gg], ug[gg]);
+                  acc[gg][0] = ffma2(b01, u2, acc[gg][0]);
+                  acc[gg][1] = ffma2(b23, u2, acc[gg][1]);
+                }
               }
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[s]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
-      }
-      if (!ok || !has) continue;
-      const float sc = p.scale_tab[k * p.L + l];
+        if (!ok || !has) continue;
 #pragma unroll
-      for (int gg = 0; gg < kDecGroup; ++gg) {
-        if (gg < nrows) {
-          float4 a = yv[gg];
-          a.x = fmaf(sc, acc[gg][0].x, a.x);
-          a.y = fmaf(sc, acc[gg][0].y, a.y);
-          a.z = fmaf(sc, acc[gg][1].x, a.z);
-          a.w = fmaf(sc, acc[gg][1].y, a.w);
-          *reinterpret_cast<float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy) = a;
+        for (int gg = 0; gg < kDecGroup; ++gg) {
+          if (gg < nrows) {
+            float4 a = yv[gg];
+            a.x = fmaf(sc, acc[gg][0].x, a.x);
+            a.y = fmaf(sc, acc[gg][0].y, a.y);
+            a.z = fmaf(sc, acc[gg][1].x, a.z);
+            a.w = fmaf(sc, acc[gg][1].y, a.w);
+            *reinterpret_cast<float4*>(ycol + (size_t)p.perm[p0 + gg] * p.ldy) = a;
+          }
         }
       }
     }

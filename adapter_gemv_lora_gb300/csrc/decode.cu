@@ -24,6 +24,8 @@
 //  * expand: u is the in-order sum of the chunk partials; v[o] accumulates
 //    B[o][i] * u[i] for i = 0..r-1 in order with fma; y = fma(scale, v, y).
 //    Each compute thread owns 4 consecutive output columns of the group's rows.
+// The fmas are issued two at a time (packed f32x2), each exactly an fmaf in
+// the order above; which CTA or work item handles a row never changes it.
 #include <cuda_runtime.h>
 
 #include "device.cuh"

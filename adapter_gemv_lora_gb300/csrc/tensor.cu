@@ -6,19 +6,21 @@
 //   expand  y_tile[128][n] += scale * (U . B[k][l]^T)        tcgen05, fp32 in TMEM
 //
 // (the delta scale * B @ (A @ x) of TensorFold PR #47; shrink then expand as in
-// xLLM PR #2014).  U stays fp32 between the kernels; for the expand it is split
-// into two bf16 halves, u_hi = bf16(u) and u_lo = bf16(u - u_hi), and both are
-// multiplied by the (exact) bf16 B and accumulated in fp32, so the rank-space
-// vector keeps about 16 significant bits.
+// xLLM PR #2014).  The shrink sums d_in in two fixed K ranges (one CTA each,
+// fp32 partials); the CTA of a tile that finishes second adds them in K order
+// and splits U into two bf16 halves, u_hi = bf16(u) and u_lo = bf16(u - u_hi),
+// stored in the layout the expand's MMA reads.  Both halves are multiplied by
+// the (exact) bf16 B and accumulated in fp32, so the rank-space vector keeps
+// about 16 significant bits.
 //
-// Kernel structure (one CTA per work item, 6 warps):
-//   warp 0   lane 0 issues TMA loads into a ring of shared-memory stages
-//   warp 1   lane 0 issues tcgen05.mma and tcgen05.commit
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows)
+// Shrink CTA (6 warps): warp 0 lane 0 issues TMA loads into a ring of
+// shared-memory stages, warp 1 lane 0 issues tcgen05.mma and tcgen05.commit,
+// warps 2-5 are the epilogue (tcgen05.ld of their 32 TMEM lanes = tile rows).
+// Expand CTA: described above tc_expand_kernel.
 // Operands: X and A tiles are K-major with the 128-byte swizzle (TMA boxes of
 // 64 bf16); B tiles are K-major with the 32-byte swizzle (boxes of 16 bf16);
-// the U halves are written by the epilogue threads in the plain K-major core
-// matrix layout (8 rows x 16 bytes per core matrix).
+// the U halves are in the plain K-major core matrix layout (8 rows x 16 bytes
+// per core matrix), bulk-copied into shared memory by the expand.
 // Each row's arithmetic is independent of every other row of its tile, and the
 // tile of a row is fixed by its own sequence, so a row's bits do not depend on
 // its batch neighbours.  Every mbarrier wait is bounded; a wait that gives up

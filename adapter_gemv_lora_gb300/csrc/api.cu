@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 #include <vector>
@@ -24,14 +25,14 @@ int cuda_status(cudaError_t e, const char* where) {
 }
 
 int sm_count(int device) {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // zero-initialised; 0 = not read yet
   if (device < 0 || device >= 64) return 148;
-  if (cache[device] == 0) {
-    int v = 0;
+  int v = cache[device].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 148;
-    cache[device] = v;
+    cache[device].store(v, std::memory_order_relaxed);
   }
-  return cache[device];
+  return v;
 }
 
 bool set_smem_limit(const void* kernel, int device, int bytes) {

@@ -532,6 +532,7 @@ def run_ours(args):
         "kernels": kernels,
         "gpu_launches": int(res["launches"]),
         "ms_per_step_eager": round(res["step_ms_eager"], 5),
+        "ms_per_step_median": round(res["step_ms_median"], 5),
         "clocks": res["clocks"],
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -558,6 +559,7 @@ def per_workload_summary(args, dev, hbm_peak):
         f = sum(u[s]["flops"] for u in units for s in STAGES)
         out[name] = {"tokens": wl.T, "ms_per_step": round(res["step_ms"], 5),
                      "ms_per_step_eager": round(res["step_ms_eager"], 5),
+                     "ms_per_step_median": round(res["step_ms_median"], 5),
                      "tokens_per_s": round(wl.T / (res["step_ms"] * 1e-3), 1),
                      "apply_ms": round(apply_ms, 5), "seg_build_ms": round(res["seg_ms"], 5),
                      "alg_bytes": int(b), "gbs": round(b / (apply_ms * 1e-3) / 1e9, 1),

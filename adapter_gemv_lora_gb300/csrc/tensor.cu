@@ -62,7 +62,7 @@ struct TcExpandParams {
   float* y;
   int32_t* status;
   int64_t ldy;
-  int L, R16, total_ng;
+  int L, R16, total_ng, tail_items;
   int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES], ng_base[LORA_MAX_LANES + 1];
 };
 
@@ -387,9 +387,17 @@ __global__ void __launch_bounds__(kExpThreads, 1)
 
   pdl_wait();  // the previous kernel's results are visible from here on
   if (*p.status != 0) return;
-  const int item = blockIdx.x;
+  // The last `tail_items` items of the step (the last wave) run as two CTAs of
+  // half the columns each, so the SMs finish closer together.
+  const int n_items = p.counts[3] * p.total_ng;
+  const int tail_start = max(0, n_items - p.tail_items);
+  int item = blockIdx.x, half = -1;
+  if (item >= tail_start) {
+    item = tail_start + (blockIdx.x - tail_start) / 2;
+    half = (blockIdx.x - tail_start) & 1;
+  }
+  if (item >= n_items) return;
   const int tile = item / p.total_ng;
-  if (tile >= p.counts[3]) return;
   const int q = item - tile * p.total_ng;
   int l = 0;
   // lane of this item, and its column range, picked with constant indexes
@@ -410,8 +418,9 @@ __global__ void __launch_bounds__(kExpThreads, 1)
   if (r <= 0) return;
   const int r16 = (r + 15) & ~15;
   const int nk = r16 / 16;
-  const int n_begin = ng * kTcNGroup;
-  const int n_end = min(d_out_l, n_begin + kTcNGroup);
+  const int n_begin = ng * kTcNGroup + (half > 0 ? kTcNGroup / 2 : 0);
+  const int n_end = min(d_out_l, ng * kTcNGroup + (half == 0 ? kTcNGroup / 2 : kTcNGroup));
+  if (n_begin >= n_end) return;  // the second half of a narrow lane's last group
   const int nchunks = (n_end - n_begin + kTcNT - 1) / kTcNT;
   const float sc = p.scale_tab[k * p.L + l];
 
@@ -677,8 +686,10 @@ int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, 
     p.ng_base[l + 1] = p.ng_base[l] + (l < pool->L ? ceil_div(pool->d_out[l], kTcNGroup) : 0);
   }
   p.total_ng = p.ng_base[pool->L];
-  const long long grid = (long long)tc_tile_bound(seg) * p.total_ng;
-  if (grid <= 0) return LORA_OK;
+  p.tail_items = sm_count(pool->device);
+  const long long items = (long long)tc_tile_bound(seg) * p.total_ng;
+  if (items <= 0) return LORA_OK;
+  const long long grid = items + p.tail_items;  // the tail's items take two CTAs each
   p.counts = seg->counts;
   p.work = seg->tc_work;
   p.rank_tab = pool->rank_tab;

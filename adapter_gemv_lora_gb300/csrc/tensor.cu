@@ -686,7 +686,7 @@ int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, 
     p.ng_base[l + 1] = p.ng_base[l] + (l < pool->L ? ceil_div(pool->d_out[l], kTcNGroup) : 0);
   }
   p.total_ng = p.ng_base[pool->L];
-  p.tail_items = sm_count(pool->device);
+  p.tail_items = sm_count(pool->device) / 2;  // half an SM wave: measured best of 0.5, 1 and 2 waves
   const long long items = (long long)tc_tile_bound(seg) * p.total_ng;
   if (items <= 0) return LORA_OK;
   const long long grid = items + p.tail_items;  // the tail's items take two CTAs each

@@ -37,9 +37,6 @@ namespace {
 constexpr int kXBoxRows = 32;                          // TMA box rows of X
 constexpr int kXStageBytes = kTcTile * kTcKBlock * 2;  // 16 KB
 constexpr int kMaxStages = 8;
-// X blocks are pulled into L2 this many k-blocks ahead of their load, which
-// keeps more HBM reads in flight than the shared-memory ring alone holds.
-constexpr int kXPrefetch = 0;
 
 struct TcShrinkParams {
   const int32_t* counts;
@@ -144,20 +141,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   if (warp == 0) {
     if (lane == 0) {
-      auto prefetch_x = [&](int kj) {
-        const int c0 = (kb_lo + kj) * kTcKBlock;
-        if (full_tile) {
-          tma_prefetch_2d(&tm_x128, c0, rb);
-        } else {
-          for (int b = 0; b < nbox; ++b) tma_prefetch_2d(&tm_x32, c0, rb + kXBoxRows * b);
-        }
-      };
-      if (kXPrefetch > 0)
-        for (int kj = stages; kj < kXPrefetch && kj < nkb; ++kj) prefetch_x(kj);
       for (int kj = 0; kj < nkb; ++kj) {
         const int kb = kb_lo + kj;
         const int s = kj % stages;
-        if (kXPrefetch > 0 && kj + kXPrefetch < nkb) prefetch_x(kj + kXPrefetch);
         if (kj >= stages) {
           if (!mbar_wait_or_fail(&empty_bar[s], ((kj / stages) - 1) & 1, &fail_sh)) {
             fail_sh = 1;

@@ -215,6 +215,19 @@ def test_row_parallel_shards_sum_to_the_delta(oracle_mod, shards):
                           f"{shards} row-parallel shards")
 
 
+def test_maximum_slot_count(oracle_mod):
+    # a pool of LORA_MAX_SLOTS slots with adapters spread over the id range,
+    # up to the last slot, on both paths
+    N = 2048
+    lens = [1, 70, 1, 1, 130, 2, 1, 64]
+    ids = [2047, 1024, 1, 0, 2046, 3, 1500, 2047]
+    rank = np.zeros((N, 1), dtype=np.int32)
+    for k in set(ids) - {0}:
+        rank[k, 0] = 4 + (k % 13)
+    wl = W.custom_workload(lens, ids, d_in=128, lane_d_out=[64], num_slots=N, max_rank=16, rank=rank, seed=21)
+    _oracle_check(oracle_mod, wl, wl.projections[0], what="2048 slots")
+
+
 @pytest.mark.parametrize("d_in", [64, 192, 1088])
 def test_k_block_counts(oracle_mod, d_in):
     # d_in of 1, 3 and 17 blocks of 64: the tensor shrink's two K ranges are

@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kSegThreads = 512;  // fewer threads, cheaper barriers: measured faster than 256 or 1024
 static_assert(kSegThreads >= 128 && kSegThreads <= 1024 && kSegThreads % 32 == 0, "block scans use 3 warps");
+constexpr int kShortSeq = 16;     // sequences up to this length are written by one thread
 // Dynamic shared memory the builder may use (227 KB per block, less its static part).
 constexpr size_t kSegSmemLimit = 227 * 1024 - 2048;
 
@@ -139,6 +140,20 @@ __device__ void block_scan3(int* a0, int n0, int* a1, int n1, int* a2, int n2, i
   t2 = sums[2][32];
 }
 
+// One warp writes dst[j] = v0 + j * step for j < n, with 16-byte stores
+// wherever the destination is aligned.
+__device__ __forceinline__ void warp_fill(int32_t* dst, int n, int v0, int step, int lane) {
+  const int head = min(n, (int)((4 - ((reinterpret_cast<uintptr_t>(dst) >> 2) & 3)) & 3));
+  if (lane < head) dst[lane] = v0 + lane * step;
+  int4* d4 = reinterpret_cast<int4*>(dst + head);
+  const int n4 = (n - head) >> 2;
+  for (int i = lane; i < n4; i += 32) {
+    const int b = v0 + (head + 4 * i) * step;
+    d4[i] = make_int4(b, b + step, b + 2 * step, b + 3 * step);
+  }
+  for (int j = head + 4 * n4 + lane; j < n; j += 32) dst[j] = v0 + j * step;
+}
+
 // Shared memory of the builder, in ints: six per-sequence arrays of S and
 // the per-key tables (2N + 2N + N + (N + 1) + (N + 1)).
 size_t seg_smem_ints(int N, int S) { return 6 * (size_t)S + 7 * (size_t)N + 2; }
@@ -157,8 +172,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   int* s_start = s_id + S;         // [S] first row
   int* s_pos = s_start + S;        // [S] rank of the first row inside its (class, slot) bin
   int* s_tile = s_pos + S;         // [S] rank of the first tile inside its slot's tiles
-  int* s_key = s_tile + S;         // [S] (class, slot) key, -1 if the sequence is inactive; bit 30: last of
-                                   //     its key in its warp
+  int* s_key = s_tile + S;         // [S] (class, slot) key, -1 if the sequence is inactive; bits 24..28:
+                                   //     the last lane of its warp with the same key
   int* cnt_tok = s_key + S;        // [2N] rows per (class, slot), then their first perm position
   int* run_tok = cnt_tok + 2 * N;  // [2N] running position while ranking sequences
   int* cnt_tile = run_tok + 2 * N; // [N]  class-1 tiles per slot, then the first tile index
@@ -166,7 +181,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   int* tc_cnt = dec_cnt + N + 1;   // [N+1] class-1 tiles per slot (scan input), then the first tile
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kLastBit = 1 << 30;
+  constexpr int kLeadShift = 24, kKeyMask = (1 << kLeadShift) - 1;  // keys < 2N <= 4096
 
   // ---- load the sequences once; validation by block reductions
   for (int i = tid; i < 2 * N; i += kSegThreads) run_tok[i] = 0;
@@ -220,8 +235,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
     }
     int tot;
     const int ex = block_exclusive_scan(s < S ? len : 0, scan_sums[0], tot);
-    int pl = 0, pt = 0;
-    bool last = true;
+    int pl = 0, pt = 0, lead = lane;
 #pragma unroll 4
     for (int j = 0; j < 32; ++j) {
       const int kj = __shfl_sync(0xffffffffu, key, j);
@@ -232,7 +246,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
           pl += lj;
           pt += tj;
         } else if (j > lane) {
-          last = false;
+          lead = j;
         }
       }
     }
@@ -241,7 +255,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
       p.seq_start[s] = carry + ex;
       s_pos[s] = pl;
       s_tile[s] = pt;
-      s_key[s] = key < 0 ? -1 : (key | (last ? kLastBit : 0));
+      s_key[s] = key < 0 ? -1 : (key | (lead << kLeadShift));
     }
     carry += tot;
   }
@@ -253,27 +267,31 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   // the tiles per slot
   if (warp == 0) {
     for (int b = 0; b < S; b += 32) {
-      const int s = b + lane;
-      const int kk = s < S ? s_key[s] : -1;
-      const int key = kk < 0 ? -1 : (kk & (kLastBit - 1));
-      const int id = key < 0 ? 0 : (key >= N ? key - N : key);
-      const bool tc = key >= N;
-      int base_tok = 0, base_tile = 0;
-      if (key >= 0) {
-        base_tok = run_tok[key];
-        if (tc) base_tile = cnt_tile[id];
+      const int s = b + lane, sc = min(s, S - 1);
+      const int kk = s_key[sc], pl = s_pos[sc], pt = s_tile[sc], len = s_len[sc];
+      const bool act = s < S && kk >= 0;
+      const int key = act ? (kk & kKeyMask) : 0;
+      const int lead = act ? (kk >> kLeadShift) : lane;
+      const bool tc = key >= N, last = act && lead == lane;
+      const int id = tc ? key - N : key;
+      // the last lane of each key reads and advances the running counts; the
+      // other lanes of the key take the base from it
+      int rt = 0, ct = 0;
+      if (last) {
+        rt = run_tok[key];
+        ct = cnt_tile[id];
       }
-      __syncwarp();
-      if (key >= 0) {
-        const int pl = s_pos[s], pt = s_tile[s];
+      const int base_tok = __shfl_sync(0xffffffffu, rt, lead);
+      const int base_tile = __shfl_sync(0xffffffffu, ct, lead);
+      if (act) {
         s_pos[s] = base_tok + pl;
         if (tc) s_tile[s] = base_tile + pt;
-        if (kk & kLastBit) {
-          run_tok[key] = base_tok + pl + s_len[s];
-          if (tc) cnt_tile[id] = base_tile + pt + (s_len[s] + kTcTile - 1) / kTcTile;
-        }
       }
-      __syncwarp();
+      if (last) {
+        run_tok[key] = base_tok + pl + len;
+        if (tc) cnt_tile[id] = base_tile + pt + (len + kTcTile - 1) / kTcTile;
+      }
+      __syncwarp();  // this chunk's counts are visible to the next chunk's reads
     }
   }
   __syncthreads();
@@ -299,15 +317,37 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
     p.seg_off[i] = (k < N) ? cnt_tok[c * N + k] : (c == 0 ? cnt_tok[N] : n_active);
   }
 
-  // ---- per-token slot and perm: one warp per sequence, coalesced writes
-  for (int s = warp; s < S; s += kSegThreads / 32) {
-    const int id = s_id[s], st = s_start[s], len = s_len[s];
-    const int kk = s_key[s];
-    const int pos = kk < 0 ? 0 : cnt_tok[kk & (kLastBit - 1)] + s_pos[s];
-    for (int j = lane; j < len; j += 32) {
-      p.slot[st + j] = id;
-      if (kk >= 0) p.perm[pos + j] = st + j;
+  // ---- per-token slot and perm, and the tensor tiles.  A thread writes the
+  // rows of each short sequence it owns (decode rows); the longer ones are
+  // dealt out to the warps in index order, one warp to a sequence.
+  for (int s = tid; s < S; s += kSegThreads) {
+    const int kk = s_key[s], len = s_len[s], id = s_id[s], st = s_start[s];
+    if (len <= kShortSeq) {
+      const int pos = kk < 0 ? 0 : cnt_tok[kk & kKeyMask] + s_pos[s];
+      for (int j = 0; j < len; ++j) {
+        p.slot[st + j] = id;
+        if (kk >= 0) p.perm[pos + j] = st + j;
+      }
     }
+    // each class-1 sequence cut into tiles of <= kTcTile rows
+    if (kk >= 0 && (kk & kKeyMask) >= N) {
+      const int base = tc_cnt[id] + s_tile[s];
+      for (int i = 0, rb = st; rb < st + len; ++i, rb += kTcTile)
+        p.tc_work[base + i] = make_int4(id, rb, min(rb + kTcTile, st + len), s);
+    }
+  }
+  int n_long = 0;  // long sequences in the chunks before this one, the same count in every warp
+  for (int c = 0; c < S; c += 32) {
+    const unsigned m = __ballot_sync(0xffffffffu, c + lane < S && s_len[c + lane] > kShortSeq);
+    int r = 0;
+    for (unsigned mm = m; mm; mm &= mm - 1, ++r) {
+      if ((n_long + r) % (kSegThreads / 32) != warp) continue;
+      const int s = c + __ffs(mm) - 1;
+      const int id = s_id[s], st = s_start[s], len = s_len[s], kk = s_key[s];
+      warp_fill(p.slot + st, len, id, 0, lane);
+      if (kk >= 0) warp_fill(p.perm + cnt_tok[kk & kKeyMask] + s_pos[s], len, st, 1, lane);
+    }
+    n_long += r;
   }
 
   // ---- decode groups: slot k's class-0 run cut into runs of <= kDecGroup
@@ -322,17 +362,6 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
     const int pb = cnt_tok[k] + gi * kDecGroup;
     const int pe = min(pb + kDecGroup, cnt_tok[k] + run_tok[k]);
     p.dec_work[w] = make_int4(k, pb, pe, 0);
-  }
-
-  // ---- tensor tiles: each class-1 sequence cut into tiles of <= kTcTile rows
-  for (int s = tid; s < S; s += kSegThreads) {
-    const int kk = s_key[s];
-    if (kk >= 0 && (kk & (kLastBit - 1)) >= N) {
-      const int id = s_id[s], st = s_start[s], len = s_len[s];
-      const int base = tc_cnt[id] + s_tile[s];
-      for (int i = 0, rb = st; rb < st + len; ++i, rb += kTcTile)
-        p.tc_work[base + i] = make_int4(id, rb, min(rb + kTcTile, st + len), s);
-    }
   }
 
   if (tid == 0) {

@@ -15,12 +15,15 @@
 // registers / shared memory for the whole stream.
 //
 // Fixed summation order, independent of the group a row lands in:
-//  * shrink: d_in is cut into 1024-wide chunks (one work item each).  Inside a
-//    chunk lane `ln` of warp `w` owns the 8 elements at k = 256*w + 8*ln,
-//    accumulated in order with fma; the 32 lanes are combined by a fixed xor
-//    butterfly (16,8,4,2,1) and the 4 warps left to right.  The chunks'
-//    partial sums go to the pool's scratch and the expand kernel adds them in
-//    chunk order.
+//  * shrink: d_in is cut into 1024-wide chunks (one work item each).  The
+//    slot's rank rows are taken in blocks of up to 32, each block in groups
+//    of 4 (nig groups, a power of two); the chunk's 8-element K blocks are
+//    dealt to nks = 128 / nig K splits: split s takes blocks s, s + nks, ....
+//    In each block the even and the odd elements feed two fma chains, added
+//    when the chunk is done; the splits are then combined by a fixed xor
+//    butterfly over the lanes of a warp and, where a group spans several
+//    warps, the warps left to right.  The chunks' partial sums go to the
+//    pool's scratch and the expand kernel adds them in chunk order.
 //  * expand: u is the in-order sum of the chunk partials; v[o] accumulates
 //    B[o][i] * u[i] for i = 0..r-1 in order with fma; y = fma(scale, v, y).
 //    Each compute thread owns 4 consecutive output columns of the group's rows.
@@ -34,15 +37,17 @@
 namespace lora {
 namespace {
 
-constexpr int kShWarps = 4;                      // shrink compute warps (256 k each)
+constexpr int kShWarps = 4;                      // shrink compute warps
 constexpr int kShThreads = (kShWarps + 1) * 32;  // + 1 producer warp
-constexpr int kShRows = 8;                       // rank rows per ring stage
-constexpr int kShStages = 4;
-constexpr int kShMaxRb = 128 / kShRows;          // rank blocks for r <= 128
-constexpr size_t kShRingBytes = (size_t)kShStages * kShRows * kDecKChunk * 2;  // 64 KB
-constexpr size_t kShRedBytes = (size_t)kShWarps * kShMaxRb * 64 * 4;          // 16 KB
-constexpr size_t kShXBytes = (size_t)2 * kDecGroup * kDecKChunk * 2;           // 32 KB, x rows, two items
-static_assert(kShWarps * 256 == kDecKChunk, "one 8-element slice per lane covers a chunk");
+constexpr int kShCompute = kShWarps * 32;        // compute threads: rank groups x K splits
+constexpr int kShStageBytes = 32768;             // A rows of one ring stage
+constexpr int kShStages = 2;
+constexpr size_t kShRingBytes = (size_t)kShStages * kShStageBytes;          // 64 KB
+constexpr size_t kShXBytes = (size_t)kDecGroup * kDecKChunk * 2;            // 16 KB, the item's x rows (bf16)
+constexpr size_t kShXfBytes = (size_t)kDecGroup * kDecKChunk * 4;           // 32 KB, the same rows in fp32
+constexpr int kShRankBlock = 32;                 // rank rows per thread-tile pass
+static_assert(kShCompute == 128 && kDecKChunk / 8 == kShCompute, "thread tiles: 128 threads, one K block each");
+static_assert(kShRankBlock * 512 * 2 <= kShStageBytes, "a 32-row block streams 512-element stages");
 
 constexpr int kExWarps = 8;                      // expand compute warps (4 columns per thread)
 constexpr int kExThreads = (kExWarps + 1) * 32;
@@ -143,6 +148,29 @@ __device__ __forceinline__ void pick_item_lane(const DecParams& p, const ExGeom&
   }
 }
 
+// Thread tiles of a shrink item.  Its rank rows are taken in blocks of up to
+// 32 (rb_rows, a multiple of 4; rows past r read the pool's zero padding),
+// each block streamed over the item's K chunk in ring stages of rb_rows x kst
+// elements.  Inside a block the rows form nig groups of 4 (a power of two)
+// and the chunk's 8-element K blocks are dealt to nks = 128 / nig K splits:
+// compute thread t takes group t / nks and the K blocks t % nks, t % nks +
+// nks, ... .  The nks splits of a group sit in one warp (nks <= 32) or in
+// nks / 32 consecutive warps.
+struct ShGeom {
+  int rows, nig, nks, kst, kbps;
+};
+
+__device__ __forceinline__ ShGeom sh_geom(int r4, int rb) {
+  ShGeom g;
+  g.rows = min(kShRankBlock, r4 - rb * kShRankBlock);
+  g.nig = 1;
+  while (g.nig * 4 < g.rows) g.nig *= 2;
+  g.nks = kShCompute / g.nig;
+  g.kst = min(kDecKChunk, kShStageBytes / (8 * g.nig));  // rows x kst bf16 <= one stage
+  g.kbps = (g.kst / 8) / g.nks;                          // K blocks per thread per stage
+  return g;
+}
+
 // One step of a butterfly reduce-scatter: lanes exchange half of their values
 // with lane ^ o and keep the sum of the half selected by bit o of their id.
 template <int HALF>
@@ -158,11 +186,13 @@ __device__ __forceinline__ void rs_step(float* v, int lane, int o) {
 
 __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* ring = reinterpret_cast<uint16_t*>(smem);         // [stage][row][kDecKChunk]
-  float* red = reinterpret_cast<float*>(smem + kShRingBytes);  // [warp][rank block][64]
-  uint16_t* xbuf = reinterpret_cast<uint16_t*>(smem + kShRingBytes + kShRedBytes);  // [2][row][kDecKChunk]
-  __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages], xfull[2], xempty[2];
-  __shared__ int4 sitem[2];  // {rank | rows << 8 | lane << 16 (0 = no more items), K chunk, first perm row, -}
+  uint16_t* ring = reinterpret_cast<uint16_t*>(smem);                        // [stage][rows][kst]
+  uint16_t* xbuf = reinterpret_cast<uint16_t*>(smem + kShRingBytes);         // [row][kDecKChunk] bf16
+  const float4* xf = reinterpret_cast<const float4*>(smem + kShRingBytes + kShXBytes);  // [row][half][K block]
+  float4* xfw = reinterpret_cast<float4*>(smem + kShRingBytes + kShXBytes);
+  __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages], xfull, xempty;
+  __shared__ int4 sitem;  // {rank | rows << 8 | lane << 16 (0 = no more items), K chunk, first perm row, -}
+  __shared__ float wsum[kShWarps][32];  // per-warp sums when a rank group spans several warps
   __shared__ int fail_sh;
 
   pdl_wait();  // the previous kernel's results are visible from here on
@@ -179,10 +209,8 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kShWarps);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&xfull[s], 1);
-      mbar_init(&xempty[s], kShWarps);
-    }
+    mbar_init(&xfull, 1);
+    mbar_init(&xempty, 1);
     fail_sh = 0;
     fence_mbar_init();
   }
@@ -204,43 +232,46 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
           r = p.rank_tab[g.x * p.L + l];
           if (r > 0) break;
         }
-        const int xs = xj & 1;
-        if (xj >= 2 && !mbar_wait_or_fail(&xempty[xs], ((xj >> 1) - 1) & 1, &fail_sh)) {
+        if (xj >= 1 && !mbar_wait_or_fail(&xempty, (xj - 1) & 1, &fail_sh)) {
           fail_sh = 1;
           break;
         }
-        if (item >= n_items) {  // no more items: an empty buffer tells the compute warps
-          sitem[xs] = make_int4(0, 0, 0, 0);
-          mbar_arrive(&xfull[xs]);
+        if (item >= n_items) {  // no more items: an empty item tells the compute warps
+          sitem = make_int4(0, 0, 0, 0);
+          mbar_arrive(&xfull);
           break;
         }
         const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
         const int nrows = g.z - g.y;
-        sitem[xs] = make_int4(r | (nrows << 8) | (l << 16), c, g.y, 0);
+        sitem = make_int4(r | (nrows << 8) | (l << 16), c, g.y, 0);
         int row[kDecGroup];  // all row indexes first: the copies below are ordered memory operations
 #pragma unroll
         for (int gg = 0; gg < kDecGroup; ++gg) row[gg] = gg < nrows ? p.perm[g.y + gg] : 0;
-        mbar_expect_tx(&xfull[xs], (uint32_t)(nrows * klen * 2));
+        mbar_expect_tx(&xfull, (uint32_t)(nrows * klen * 2));
 #pragma unroll
         for (int gg = 0; gg < kDecGroup; ++gg)
           if (gg < nrows)
-            bulk_load(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk, p.x + (size_t)row[gg] * p.ldx + k0,
-                      (uint32_t)(klen * 2), &xfull[xs]);
+            bulk_load(xbuf + (size_t)gg * kDecKChunk, p.x + (size_t)row[gg] * p.ldx + k0, (uint32_t)(klen * 2), &xfull);
         ++xj;
+        const int r4 = (r + 3) & ~3;
         const uint16_t* Ab = lane_param(p.A, l) + (size_t)g.x * p.R16 * p.d_in + k0;
         bool ok = true;
-        for (int rb = 0; rb < r; rb += kShRows, ++fill) {
-          const int s = fill % kShStages;
-          if (fill >= kShStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kShStages) - 1) & 1, &fail_sh)) {
-            ok = false;
-            fail_sh = 1;
-            break;
+        for (int rb = 0; rb * kShRankBlock < r4 && ok; ++rb) {
+          const ShGeom sg = sh_geom(r4, rb);
+          const uint16_t* Arb = Ab + (size_t)rb * kShRankBlock * p.d_in;
+          for (int ks0 = 0; ks0 < klen; ks0 += sg.kst, ++fill) {
+            const int s = fill % kShStages;
+            if (fill >= kShStages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kShStages) - 1) & 1, &fail_sh)) {
+              ok = false;
+              fail_sh = 1;
+              break;
+            }
+            const int kl = min(sg.kst, klen - ks0);
+            mbar_expect_tx(&full_bar[s], (uint32_t)(sg.rows * kl * 2));
+            uint16_t* dst = ring + (size_t)s * (kShStageBytes / 2);
+            for (int i = 0; i < sg.rows; ++i)
+              bulk_load(dst + (size_t)i * sg.kst, Arb + (size_t)i * p.d_in + ks0, (uint32_t)(kl * 2), &full_bar[s]);
           }
-          const int rows = min(kShRows, r - rb);
-          mbar_expect_tx(&full_bar[s], (uint32_t)(rows * klen * 2));
-          for (int i = 0; i < rows; ++i)
-            bulk_load(ring + ((size_t)s * kShRows + i) * kDecKChunk, Ab + (size_t)(rb + i) * p.d_in,
-                      (uint32_t)(klen * 2), &full_bar[s]);
         }
         if (!ok) break;
         item = next_item(p.sched);
@@ -248,103 +279,123 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
       finish_items(p.sched, min((int)gridDim.x, n_items));
     }
   } else {
-    // ---------------- compute warps: the items the producer hands over with their x rows
+    // ---------------- compute warps
     uint32_t use = 0, xj = 0;
-    bool ok = true;
-    const int kk = warp * 256 + lane * 8;
+    const int t = tid;
     for (;;) {
-      const int xs = xj & 1;
-      if (!ok || !mbar_wait_or_fail(&xfull[xs], (xj >> 1) & 1, &fail_sh)) {
-        fail_sh = 1;
-        break;
-      }
-      const int4 it = sitem[xs];
+      if (!mbar_wait_or_fail(&xfull, xj & 1, &fail_sh)) fail_sh = 1;
+      const int4 it = sitem;
+      named_bar_sync(1, kShCompute);  // every compute thread has its verdict and the item
+      if (fail_sh) break;
       const int r = it.x & 0xff, nrows = (it.x >> 8) & 0xff, l = it.x >> 16, c = it.y, p0 = it.z;
       if (r <= 0) break;  // no more items
-      const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
-      const bool has_k = kk < klen;
-      // x of rows 2p and 2p+1 side by side, for the packed fma
-      float2 xp[kDecGroup / 2][8];
+      const int klen = min(kDecKChunk, p.d_in - c * kDecKChunk);
+      // x rows to fp32, split into the two halves of each 8-element K block so
+      // that the fma loop reads consecutive 16-byte words across threads
 #pragma unroll
-      for (int pp = 0; pp < kDecGroup / 2; ++pp) {
-        float xv[2][8];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int gg = 2 * pp + h;
-          if (ok && gg < nrows && has_k) {
-            unpack8(*reinterpret_cast<const uint4*>(xbuf + ((size_t)xs * kDecGroup + gg) * kDecKChunk + kk), xv[h]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xv[h][e] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xp[pp][e] = make_float2(xv[0][e], xv[1][e]);
+      for (int gg = 0; gg < kDecGroup; ++gg) {
+        float v[8];
+        unpack8(*reinterpret_cast<const uint4*>(xbuf + (size_t)gg * kDecKChunk + 8 * t), v);
+        xfw[(gg * 2 + 0) * (kDecKChunk / 8) + t] = make_float4(v[0], v[1], v[2], v[3]);
+        xfw[(gg * 2 + 1) * (kDecKChunk / 8) + t] = make_float4(v[4], v[5], v[6], v[7]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xempty[xs]);
+      named_bar_sync(1, kShCompute);  // fp32 rows complete; the bf16 buffer may be refilled
+      if (t == 0) mbar_arrive(&xempty);
       ++xj;
-      const int nrb = (r + kShRows - 1) / kShRows;
-      for (int rb = 0; rb < nrb; ++rb, ++use) {
-        const int s = use % kShStages;
-        if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kShStages) & 1, &fail_sh)) {
-          ok = false;
-          fail_sh = 1;
-        }
-        // acc2[pp][i] = partial sums of rank row i for rows (2pp, 2pp+1); each
-        // is the in-order fma chain over the lane's 8 elements
-        float2 acc2[kDecGroup / 2][kShRows];
+      const int r4 = (r + 3) & ~3;
+      bool ok = true;
+      for (int rb = 0; rb * kShRankBlock < r4; ++rb) {
+        const ShGeom sg = sh_geom(r4, rb);
+        const int ig = t / sg.nks, ks = t - ig * sg.nks;
+        const bool active = ig * 4 < sg.rows;
+        // acc[row][j] = (sum over even k, sum over odd k) of A[4 ig + j][k] * x[row][k]
+        float2 acc[kDecGroup][4];
 #pragma unroll
-        for (int pp = 0; pp < kDecGroup / 2; ++pp)
+        for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
-          for (int i = 0; i < kShRows; ++i) acc2[pp][i] = make_float2(0.f, 0.f);
-        if (ok && has_k) {
-          const uint16_t* st = ring + (size_t)s * kShRows * kDecKChunk + kk;
+          for (int j = 0; j < 4; ++j) acc[gg][j] = make_float2(0.f, 0.f);
+        for (int ks0 = 0; ks0 < klen; ks0 += sg.kst, ++use) {
+          const int s = use % kShStages;
+          if (!mbar_wait_or_fail(&full_bar[s], (use / kShStages) & 1, &fail_sh)) {
+            ok = false;
+            fail_sh = 1;
+          }
+          if (ok && active) {
+            const int kl = min(sg.kst, klen - ks0);
+            const uint16_t* As = ring + (size_t)s * (kShStageBytes / 2) + (size_t)(4 * ig) * sg.kst;
+            for (int jb = 0; jb < sg.kbps; ++jb) {
+              const int kloc = 8 * (ks + jb * sg.nks);
+              if (kloc >= kl) break;
+              float2 a[4][4];
 #pragma unroll
-          for (int i = 0; i < kShRows; ++i) {
-            if (rb * kShRows + i < r) {
-              float av[8];
-              unpack8(*reinterpret_cast<const uint4*>(st + (size_t)i * kDecKChunk), av);
+              for (int j = 0; j < 4; ++j) {
+                const uint4 q = *reinterpret_cast<const uint4*>(As + (size_t)j * sg.kst + kloc);
+                a[j][0] = make_float2(bf16lo(q.x), bf16hi(q.x));
+                a[j][1] = make_float2(bf16lo(q.y), bf16hi(q.y));
+                a[j][2] = make_float2(bf16lo(q.z), bf16hi(q.z));
+                a[j][3] = make_float2(bf16lo(q.w), bf16hi(q.w));
+              }
+              const int kb = (ks0 + kloc) >> 3;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float2 a2 = make_float2(av[e], av[e]);
+              for (int gg = 0; gg < kDecGroup; ++gg) {
+                const float4 x0 = xf[(gg * 2 + 0) * (kDecKChunk / 8) + kb];
+                const float4 x1 = xf[(gg * 2 + 1) * (kDecKChunk / 8) + kb];
+                const float2 xp[4] = {make_float2(x0.x, x0.y), make_float2(x0.z, x0.w), make_float2(x1.x, x1.y),
+                                      make_float2(x1.z, x1.w)};
 #pragma unroll
-                for (int pp = 0; pp < kDecGroup / 2; ++pp) acc2[pp][i] = ffma2(a2, xp[pp][e], acc2[pp][i]);
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) acc[gg][j] = ffma2(a[j][e], xp[e], acc[gg][j]);
               }
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[s]);
         }
-        float acc[kDecGroup * 8];  // index gg*8 + i
+        // the K splits' sums: a fixed butterfly over the lanes of a group, then
+        // (groups spanning several warps) the warps in order
+        float v[32];  // index row * 4 + j
 #pragma unroll
-        for (int pp = 0; pp < kDecGroup / 2; ++pp)
+        for (int gg = 0; gg < kDecGroup; ++gg)
 #pragma unroll
-          for (int i = 0; i < kShRows; ++i) {
-            acc[(2 * pp) * 8 + i] = acc2[pp][i].x;
-            acc[(2 * pp + 1) * 8 + i] = acc2[pp][i].y;
+          for (int j = 0; j < 4; ++j) v[gg * 4 + j] = acc[gg][j].x + acc[gg][j].y;
+        int out0, nout;  // this lane's outputs: v[0 .. nout) are outputs out0, out0 + 1, ...
+        if (sg.nks == 16) {
+          rs_step<16>(v, lane, 8);
+          rs_step<8>(v, lane, 4);
+          rs_step<4>(v, lane, 2);
+          rs_step<2>(v, lane, 1);
+          out0 = 2 * (lane & 15);
+          nout = 2;
+        } else {
+          rs_step<16>(v, lane, 16);
+          rs_step<8>(v, lane, 8);
+          rs_step<4>(v, lane, 4);
+          rs_step<2>(v, lane, 2);
+          rs_step<1>(v, lane, 1);
+          out0 = lane;
+          nout = 1;
+        }
+        bool writer = true;
+        if (sg.nks > 32) {
+          const int wpg = sg.nks / 32;  // warps per rank group
+          wsum[warp][lane] = v[0];
+          named_bar_sync(1, kShCompute);
+          writer = warp % wpg == 0;
+          if (writer) {
+            float sum = wsum[warp][lane];
+            for (int ww = 1; ww < wpg; ++ww) sum += wsum[warp + ww][lane];
+            v[0] = sum;
           }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
-        rs_step<32>(acc, lane, 16);
-        rs_step<16>(acc, lane, 8);
-        rs_step<8>(acc, lane, 4);
-        rs_step<4>(acc, lane, 2);
-        rs_step<2>(acc, lane, 1);
-        // lane now holds the warp sums of values 2*lane and 2*lane+1
-        float* rw = red + ((size_t)warp * kShMaxRb + rb) * 64;
-        rw[2 * lane] = acc[0];
-        rw[2 * lane + 1] = acc[1];
-      }
-      named_bar_sync(1, kShWarps * 32);
-      for (int idx = tid; idx < nrb * 64; idx += kShWarps * 32) {
-        const int rb = idx >> 6, v = idx & 63, gg = v >> 3, i = v & 7;
-        if (gg < nrows && rb * kShRows + i < r) {
-          float sum = red[(size_t)rb * 64 + v];
-#pragma unroll
-          for (int ww = 1; ww < kShWarps; ++ww) sum += red[((size_t)ww * kShMaxRb + rb) * 64 + v];
-          p.u_dec[(((size_t)c * p.max_tokens + p0 + gg) * p.L + l) * p.R16 + rb * kShRows + i] = sum;
+          named_bar_sync(1, kShCompute);  // wsum is read before the next block writes it
+        }
+        if (ok && writer) {
+          for (int e = 0; e < nout; ++e) {
+            const int o = out0 + e, gg = o >> 2, i = rb * kShRankBlock + 4 * ig + (o & 3);
+            if (gg < nrows && i < r) p.u_dec[(((size_t)c * p.max_tokens + p0 + gg) * p.L + l) * p.R16 + i] = v[e];
+          }
         }
       }
-      named_bar_sync(1, kShWarps * 32);
     }
   }
   __syncthreads();
@@ -548,7 +599,7 @@ int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uin
   const long long cap = 2LL * sm_count(pool->device);
   const int grid = (int)(items < cap ? items : cap);
   if (grid <= 0) return LORA_OK;
-  const int smem = (int)(kShRingBytes + kShRedBytes + kShXBytes);
+  const int smem = (int)(kShRingBytes + kShXBytes + kShXfBytes);
   if (!set_smem_limit(reinterpret_cast<const void*>(dec_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
   const cudaError_t e = launch_pdl(dec_shrink_kernel, dim3(grid), dim3(kShThreads), smem, st, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);

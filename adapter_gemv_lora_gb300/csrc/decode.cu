@@ -184,7 +184,7 @@ __device__ __forceinline__ void rs_step(float* v, int lane, int o) {
   }
 }
 
-__global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
+__global__ void __launch_bounds__(kShThreads, 2) dec_shrink_kernel(DecParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* ring = reinterpret_cast<uint16_t*>(smem);                        // [stage][rows][kst]
   uint16_t* xbuf = reinterpret_cast<uint16_t*>(smem + kShRingBytes);         // [row][kDecKChunk] bf16
@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
   __shared__ __align__(8) uint64_t full_bar[kShStages], empty_bar[kShStages], xfull, xempty;
   __shared__ int4 sitem;  // {rank | rows << 8 | lane << 16 (0 = no more items), K chunk, first perm row, -}
   __shared__ float wsum[kShWarps][32];  // per-warp sums when a rank group spans several warps
+  __shared__ int stop_sh[2];            // per item parity: the compute warps leave the loop
   __shared__ int fail_sh;
 
   pdl_wait();  // the previous kernel's results are visible from here on
@@ -285,10 +286,11 @@ __global__ void __launch_bounds__(kShThreads) dec_shrink_kernel(DecParams p) {
     for (;;) {
       if (!mbar_wait_or_fail(&xfull, xj & 1, &fail_sh)) fail_sh = 1;
       const int4 it = sitem;
-      named_bar_sync(1, kShCompute);  // every compute thread has its verdict and the item
-      if (fail_sh) break;
+      named_bar_sync(1, kShCompute);  // every compute thread has waited (failures recorded)
+      if (t == 0) stop_sh[xj & 1] = fail_sh || (it.x & 0xff) == 0;  // a failure, or no more items
+      named_bar_sync(1, kShCompute);  // one decision for all compute threads
+      if (stop_sh[xj & 1]) break;
       const int r = it.x & 0xff, nrows = (it.x >> 8) & 0xff, l = it.x >> 16, c = it.y, p0 = it.z;
-      if (r <= 0) break;  // no more items
       const int klen = min(kDecKChunk, p.d_in - c * kDecKChunk);
       // x rows to fp32, split into the two halves of each 8-element K block so
       // that the fma loop reads consecutive 16-byte words across threads

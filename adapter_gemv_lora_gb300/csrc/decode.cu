@@ -8,11 +8,11 @@
 //           scale * B @ (A @ x); xLLM PR #2014, shrink then expand)
 //
 // Both kernels are HBM streams of factor rows: a producer warp copies the
-// slot's rank rows (A rows for the shrink, B^T rows for the expand; true rank
-// only, never the padding) with the TMA bulk-copy engine into a ring of
-// shared-memory stages, and the compute warps consume them with 128-bit
-// shared loads.  The group's x rows (shrink) or u vectors (expand) stay in
-// registers / shared memory for the whole stream.
+// slot's rank rows (A rows for the shrink, the true rank rounded up to 4;
+// B^T rows for the expand, the true rank) with the TMA bulk-copy engine into
+// a ring of shared-memory stages, and the compute warps consume them with
+// 128-bit shared loads.  The group's x rows (shrink, converted once to fp32)
+// and u vectors (expand) stay in shared memory for the whole stream.
 //
 // Fixed summation order, independent of the group a row lands in:
 //  * shrink: d_in is cut into 1024-wide chunks (one work item each).  The

@@ -241,6 +241,33 @@ def test_k_block_counts(oracle_mod, d_in):
     _oracle_check(oracle_mod, wl, wl.projections[0], what=f"d_in={d_in}")
 
 
+@pytest.mark.parametrize("lanes", [[256], [128, 64]])
+def test_decode_rank_geometry(oracle_mod, lanes):
+    # the decode shrink cuts a slot's rank rows into blocks of up to 32 and each
+    # block into groups of 4 (their count rounded up to a power of two) and
+    # deals the K blocks to 128 / groups splits: one slot per geometry, ranks
+    # 1..128 with 4-row tails past a 32-row block, decode rows in groups of 1 to
+    # 8 rows, and a ragged last K chunk (2112 = 2 x 1024 + 64); every row
+    # against the oracle
+    ranks = [1, 3, 4, 5, 8, 9, 12, 16, 17, 20, 31, 32, 33, 36, 48, 64, 65, 96, 100, 127, 128]
+    N = len(ranks) + 1
+    L = len(lanes)
+    rank = np.zeros((N, L), dtype=np.int32)
+    for k, r in enumerate(ranks, start=1):
+        rank[k, :] = r
+        if L > 1:
+            rank[k, 1] = ranks[(k * 7) % len(ranks)]
+    lens, ids = [], []
+    for k in range(1, N):
+        for _ in range(1 + (k * 3) % 8):  # 1..8 single-token rows of slot k
+            lens.append(1)
+            ids.append(k)
+    lens += [1, 1, 5, 2]
+    ids += [0, 3, 7, 0]
+    wl = W.custom_workload(lens, ids, d_in=2112, lane_d_out=lanes, num_slots=N, max_rank=128, rank=rank, seed=77)
+    _oracle_check(oracle_mod, wl, wl.projections[0], what=f"rank geometry, lanes {lanes}")
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode_oproj"])
 def test_decode_configs_full(oracle_mod, name):
     wl = W.make_workload(name)

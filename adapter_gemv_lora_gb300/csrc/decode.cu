@@ -60,6 +60,7 @@ static_assert(kExWarps * 32 * kExCols == kDecNChunk, "the compute threads cover 
 struct DecParams {
   const int32_t* counts;
   const int4* work;
+  const int4* dec_rows;  // [group][2]: the group's 8 row indexes (entries past its row count unused)
   const int32_t* perm;
   const int32_t* rank_tab;
   const float* scale_tab;
@@ -224,12 +225,14 @@ __global__ void __launch_bounds__(kShThreads, 2) dec_shrink_kernel(DecParams p) 
       int item = blockIdx.x;
       for (;;) {
         int r = 0, l = 0, c = 0;
-        int4 g = make_int4(0, 0, 0, 0);
+        int4 g = make_int4(0, 0, 0, 0), rw0 = g, rw1 = g;
         for (; item < n_items; item = next_item(p.sched)) {  // items of a rank-0 lane do nothing
           const int w = item / per_group, rem = item - w * per_group;
           l = rem / p.C;
           c = rem - l * p.C;
-          g = p.work[w];
+          g = p.work[w];  // the group and its rows load together; the rank follows the group
+          rw0 = p.dec_rows[2 * w];
+          rw1 = p.dec_rows[2 * w + 1];
           r = p.rank_tab[g.x * p.L + l];
           if (r > 0) break;
         }
@@ -245,9 +248,7 @@ __global__ void __launch_bounds__(kShThreads, 2) dec_shrink_kernel(DecParams p) 
         const int k0 = c * kDecKChunk, klen = min(kDecKChunk, p.d_in - k0);
         const int nrows = g.z - g.y;
         sitem = make_int4(r | (nrows << 8) | (l << 16), c, g.y, 0);
-        int row[kDecGroup];  // all row indexes first: the copies below are ordered memory operations
-#pragma unroll
-        for (int gg = 0; gg < kDecGroup; ++gg) row[gg] = gg < nrows ? p.perm[g.y + gg] : 0;
+        const int row[kDecGroup] = {rw0.x, rw0.y, rw0.z, rw0.w, rw1.x, rw1.y, rw1.z, rw1.w};
         mbar_expect_tx(&xfull, (uint32_t)(nrows * klen * 2));
 #pragma unroll
         for (int gg = 0; gg < kDecGroup; ++gg)
@@ -561,6 +562,7 @@ DecParams make_params(const lora_pool* pool, const lora_segments* seg) {
   DecParams p{};
   p.counts = seg->counts;
   p.work = seg->dec_work;
+  p.dec_rows = reinterpret_cast<const int4*>(seg->dec_rows);
   p.perm = seg->perm;
   p.status = seg->status;
   p.rank_tab = pool->rank_tab;

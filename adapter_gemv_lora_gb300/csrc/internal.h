@@ -85,6 +85,7 @@ struct lora_segments {
   int32_t* perm = nullptr;
   int32_t* seg_off = nullptr;
   int4* dec_work = nullptr;
+  int32_t* dec_rows = nullptr;  // [cap_dec][kDecGroup] the rows of each decode group (its perm entries)
   int4* tc_work = nullptr;
 };
 

@@ -40,6 +40,7 @@ struct SegParams {
   int32_t* perm;
   int32_t* seg_off;
   int4* dec_work;
+  int32_t* dec_rows;
   int4* tc_work;
 };
 
@@ -324,9 +325,12 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
     const int kk = s_key[s], len = s_len[s], id = s_id[s], st = s_start[s];
     if (len <= kShortSeq) {
       const int pos = kk < 0 ? 0 : cnt_tok[kk & kKeyMask] + s_pos[s];
+      const bool dec = kk >= 0 && (kk & kKeyMask) < N;  // decode rows also go to their group's row list
+      const int g0 = dec ? dec_cnt[kk & kKeyMask] * kDecGroup + s_pos[s] : 0;
       for (int j = 0; j < len; ++j) {
         p.slot[st + j] = id;
         if (kk >= 0) p.perm[pos + j] = st + j;
+        if (dec) p.dec_rows[g0 + j] = st + j;
       }
     }
     // each class-1 sequence cut into tiles of <= kTcTile rows
@@ -346,6 +350,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
       const int id = s_id[s], st = s_start[s], len = s_len[s], kk = s_key[s];
       warp_fill(p.slot + st, len, id, 0, lane);
       if (kk >= 0) warp_fill(p.perm + cnt_tok[kk & kKeyMask] + s_pos[s], len, st, 1, lane);
+      if (kk >= 0 && (kk & kKeyMask) < N)  // decode rows (a sequence shorter than the tensor threshold)
+        warp_fill(p.dec_rows + dec_cnt[kk & kKeyMask] * kDecGroup + s_pos[s], len, st, 1, lane);
     }
     n_long += r;
   }
@@ -390,6 +396,7 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
   p.perm = seg->perm;
   p.seg_off = seg->seg_off;
   p.dec_work = seg->dec_work;
+  p.dec_rows = seg->dec_rows;
   p.tc_work = seg->tc_work;
   const size_t sm = sizeof(int) * seg_smem_ints(seg->N, S);
   if (sm > 48 * 1024 && !set_smem_limit(reinterpret_cast<const void*>(seg_build_kernel), seg->device, (int)sm))
@@ -406,7 +413,7 @@ using namespace lora;
 namespace {
 
 struct SegLayout {
-  size_t status, counts, seq_start, slot, perm, seg_off, dec_work, tc_work, total;
+  size_t status, counts, seq_start, slot, perm, seg_off, dec_work, dec_rows, tc_work, total;
   int cap_dec, cap_tc;
 };
 
@@ -426,6 +433,7 @@ bool seg_layout(int max_seqs, int max_tokens, int N, SegLayout* L) {
   L->perm = o; o = align256(o + 4 * (size_t)max_tokens);
   L->seg_off = o; o = align256(o + 4 * (size_t)(2 * (N + 1)));
   L->dec_work = o; o = align256(o + 16 * (size_t)L->cap_dec);
+  L->dec_rows = o; o = align256(o + 4 * (size_t)kDecGroup * L->cap_dec);
   L->tc_work = o; o = align256(o + 16 * (size_t)L->cap_tc);
   L->total = o;
   return true;
@@ -466,6 +474,7 @@ int lora_segments_create(lora_segments** out, void* dev_ws, size_t ws_bytes, int
   s->perm = reinterpret_cast<int32_t*>(b + L.perm);
   s->seg_off = reinterpret_cast<int32_t*>(b + L.seg_off);
   s->dec_work = reinterpret_cast<int4*>(b + L.dec_work);
+  s->dec_rows = reinterpret_cast<int32_t*>(b + L.dec_rows);
   s->tc_work = reinterpret_cast<int4*>(b + L.tc_work);
   *out = s;
   return LORA_OK;

@@ -532,6 +532,18 @@ int lora_segments_read(const lora_segments* seg, int32_t* host_slot, int32_t* ho
   return cudaStreamSynchronize(st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
+int lora_segments_read_dec_rows(const lora_segments* seg, int32_t* host_rows, lora_stream_t stream) {
+  if (!seg || !host_rows) return LORA_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t counts[4];
+  if (cudaMemcpyAsync(counts, seg->counts, 16, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LORA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LORA_ERR_CUDA;
+  const size_t n = (size_t)std::max(0, counts[2]) * kDecGroup;
+  if (n > 0 && cudaMemcpyAsync(host_rows, seg->dec_rows, 4 * n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
 int lora_get_status(const lora_segments* seg, int32_t* host_status, lora_stream_t stream) {
   if (!seg || !host_status) return LORA_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -55,6 +55,7 @@ def load_library(path: str = LIB_PATH):
         "lora_build_segments": (I, [P, P, P, I, I, P]),
         "lora_segments_capacity": (I, [P, P, P]),
         "lora_segments_read": (I, [P, P, P, P, P, P, P, P]),
+        "lora_segments_read_dec_rows": (I, [P, P, P]),
         "lora_get_status": (I, [P, P, P]),
         "lora_clear_status": (I, [P, P]),
         "lora_segments_destroy": (I, [P]),
@@ -160,7 +161,16 @@ def lora_segments_read(seg: int, num_tokens: int, num_slots: int, stream: int = 
            "lora_segments_read")
     n_act, n_dec_rows, nd, nt = (int(c) for c in counts)
     return {"slot": slot[:num_tokens], "perm": perm[:n_act], "seg_off": seg_off, "counts": counts,
-            "dec_work": dec[:nd], "tc_work": tc[:nt]}
+            "dec_work": dec[:nd], "tc_work": tc[:nt], "dec_rows": lora_segments_read_dec_rows(seg, stream)[:nd]}
+
+
+def lora_segments_read_dec_rows(seg: int, stream: int = 0) -> np.ndarray:
+    """The last build's decode-group row lists, [capacity][8] (rows past a group's count unspecified)."""
+    dec_cap, _ = lora_segments_capacity(seg)
+    rows = np.zeros((max(dec_cap, 1), 8), dtype=np.int32)
+    _check(load_library().lora_segments_read_dec_rows(seg, rows.ctypes.data_as(ctypes.c_void_p), stream),
+           "lora_segments_read_dec_rows")
+    return rows
 
 
 def lora_get_status(seg: int, stream: int = 0) -> int:

@@ -167,6 +167,12 @@ int lora_segments_read(const lora_segments* seg, int32_t* host_slot, int32_t* ho
                        int32_t* host_seg_off, int32_t* host_counts, int32_t* host_dec_work,
                        int32_t* host_tc_work, lora_stream_t stream);
 
+/* Copy the last build's decode-group row lists to host_rows[8 * n] (n = the
+ * build's decode group count, counts[2]; tests and tools; synchronises
+ * `stream`).  Group w's rows are perm[pb .. pe) of its work entry (k, pb, pe)
+ * in order; the entries past pe - pb are unspecified. */
+int lora_segments_read_dec_rows(const lora_segments* seg, int32_t* host_rows, lora_stream_t stream);
+
 /* Read the status word (copies 4 bytes and synchronises `stream`). */
 int lora_get_status(const lora_segments* seg, int32_t* host_status, lora_stream_t stream);
 

@@ -30,6 +30,9 @@ def _compare(oracle_mod, ids, lens, N, T=None):
     assert np.array_equal(got["seg_off"], exp["seg_off"])
     assert np.array_equal(got["dec_work"], exp["dec_work"])
     assert np.array_equal(got["tc_work"], exp["tc_work"])
+    # each decode group's row list is its perm range, in order
+    for w, (_, pb, pe, _) in enumerate(exp["dec_work"]):
+        assert np.array_equal(got["dec_rows"][w, :pe - pb], exp["perm"][pb:pe]), f"group {w}"
 
 
 @pytest.mark.parametrize("seed", range(10))

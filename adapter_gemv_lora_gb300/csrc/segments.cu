@@ -340,20 +340,23 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
         p.tc_work[base + i] = make_int4(id, rb, min(rb + kTcTile, st + len), s);
     }
   }
-  int n_long = 0;  // long sequences in the chunks before this one, the same count in every warp
-  for (int c = 0; c < S; c += 32) {
-    const unsigned m = __ballot_sync(0xffffffffu, c + lane < S && s_len[c + lane] > kShortSeq);
-    int r = 0;
-    for (unsigned mm = m; mm; mm &= mm - 1, ++r) {
-      if ((n_long + r) % (kSegThreads / 32) != warp) continue;
-      const int s = c + __ffs(mm) - 1;
-      const int id = s_id[s], st = s_start[s], len = s_len[s], kk = s_key[s];
-      warp_fill(p.slot + st, len, id, 0, lane);
-      if (kk >= 0) warp_fill(p.perm + cnt_tok[kk & kKeyMask] + s_pos[s], len, st, 1, lane);
-      if (kk >= 0 && (kk & kKeyMask) < N)  // decode rows (a sequence shorter than the tensor threshold)
-        warp_fill(p.dec_rows + dec_cnt[kk & kKeyMask] * kDecGroup + s_pos[s], len, st, 1, lane);
-    }
-    n_long += r;
+  // the long sequences, compacted into a list (in s_tile, which is no longer
+  // read once the tiles above are written), then one warp to each
+  int my_long = 0;
+  for (int s = tid; s < S; s += kSegThreads) my_long += s_len[s] > kShortSeq ? 1 : 0;
+  int n_long;
+  int li = block_exclusive_scan(my_long, scan_sums[0], n_long);  // barriers: the tiles are written
+  int* long_list = s_tile;
+  for (int s = tid; s < S; s += kSegThreads)
+    if (s_len[s] > kShortSeq) long_list[li++] = s;
+  __syncthreads();
+  for (int i = warp; i < n_long; i += kSegThreads / 32) {
+    const int s = long_list[i];
+    const int id = s_id[s], st = s_start[s], len = s_len[s], kk = s_key[s];
+    warp_fill(p.slot + st, len, id, 0, lane);
+    if (kk >= 0) warp_fill(p.perm + cnt_tok[kk & kKeyMask] + s_pos[s], len, st, 1, lane);
+    if (kk >= 0 && (kk & kKeyMask) < N)  // decode rows (a sequence shorter than the tensor threshold)
+      warp_fill(p.dec_rows + dec_cnt[kk & kKeyMask] * kDecGroup + s_pos[s], len, st, 1, lane);
   }
 
   // ---- decode groups: slot k's class-0 run cut into runs of <= kDecGroup

@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
           a.y += d.y;
           a.z += d.z;
           a.w += d.w;
-          *reinterpret_cast<float4*>(p.y + (size_t)t * p.ldy + col) = a;
+          __stcs(reinterpret_cast<float4*>(p.y + (size_t)t * p.ldy + col), a);  // streaming: y is not read again
         }
       }
       __syncwarp();

@@ -94,6 +94,43 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* addr,
   return r == CUDA_SUCCESS;
 }
 
+// Host checks shared by every apply entry point (no GPU work).
+int check_apply(const lora_pool* pool, const lora_segments* seg, const void* x, const float* y, int64_t ldx,
+                int64_t ldy) {
+  if (!pool || !seg || !x || !y) return LORA_ERR_ARG;
+  const PoolView& v = pool->v;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15)) return LORA_ERR_ARG;
+  if (ldx < v.d_in || ldy < v.D || (ldx % 8) || (ldy % 4)) return LORA_ERR_ARG;
+  if (seg->N != v.N) return LORA_ERR_SHAPE;
+  if (seg->T > v.max_tokens) return LORA_ERR_SHAPE;
+  // the kernels run on the current device: the pool and the segments must live there
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  if (dev != v.device || dev != seg->device) return LORA_ERR_ARG;
+  return LORA_OK;
+}
+
+bool pool_has_adapter(const lora_pool* pool) {
+  for (int r : pool->h_rank)
+    if (r > 0) return true;
+  return false;
+}
+
+int run_stage(const PoolView& pool, const lora_segments* seg, const void* x, float* y, int64_t ldx, int64_t ldy,
+              int stage, cudaStream_t st) {
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  switch (stage) {
+    case 1:
+      return launch_decode(pool, seg, xb, ldx, y, ldy, st);
+    case 2:
+      return launch_tc_shrink(pool, seg, xb, ldx, st);
+    case 3:
+      return launch_tc_expand(pool, seg, y, ldy, st);
+    default:
+      return LORA_ERR_ARG;
+  }
+}
+
 }  // namespace lora
 
 using namespace lora;
@@ -131,63 +168,24 @@ SideStream* side_stream() {
 // yet (outside any stream capture, from pool creation).
 bool lora::ensure_side_stream() { return side_stream() != nullptr; }
 
-namespace {
-
-bool any_loaded(const lora_pool* pool) {
-  for (int v : pool->h_rank)
-    if (v > 0) return true;
-  return false;
-}
-
-int check_apply(const lora_pool* pool, const lora_segments* seg, const void* x, const float* y, int64_t ldx,
-                int64_t ldy) {
-  if (!pool || !seg || !x || !y) return LORA_ERR_ARG;
-  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15)) return LORA_ERR_ARG;
-  if (ldx < pool->d_in || ldy < pool->D || (ldx % 8) || (ldy % 4)) return LORA_ERR_ARG;
-  if (seg->N != pool->N) return LORA_ERR_SHAPE;
-  if (seg->T > pool->max_tokens) return LORA_ERR_SHAPE;
-  // the kernels run on the current device: the pool and the segments must live there
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
-  if (dev != pool->device || dev != seg->device) return LORA_ERR_ARG;
-  return LORA_OK;
-}
-
-int apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y, int64_t ldx, int64_t ldy,
-                int stage, cudaStream_t st) {
-  switch (stage) {
-    case 1:
-      return launch_dec_shrink(pool, seg, static_cast<const uint16_t*>(x), ldx, st);
-    case 2:
-      return launch_dec_expand(pool, seg, y, ldy, st);
-    case 3:
-      return launch_tc_shrink(pool, seg, static_cast<const uint16_t*>(x), ldx, st);
-    case 4:
-      return launch_tc_expand(pool, seg, y, ldy, st);
-    default:
-      return LORA_ERR_ARG;
-  }
-}
-
-}  // namespace
-
 extern "C" {
 
 int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, const void* x, float* y, int64_t ldx,
                              int64_t ldy, lora_stream_t stream) {
   const int chk = check_apply(pool, seg, x, y, ldx, ldy);
   if (chk != LORA_OK) return chk;
-  if (seg->T == 0 || !any_loaded(pool)) return LORA_OK;  // a layer no adapter edits launches nothing
+  if (seg->T == 0 || !pool_has_adapter(pool)) return LORA_OK;  // a layer no adapter edits launches nothing
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const PoolView& v = pool->v;
   SideStream* side = side_stream();
   if (!side) {
-    for (int stage = 1; stage <= 4; ++stage) {
-      const int r = apply_stage(pool, seg, x, y, ldx, ldy, stage, st);
+    for (int stage = 1; stage <= 3; ++stage) {
+      const int r = run_stage(v, seg, x, y, ldx, ldy, stage, st);
       if (r != LORA_OK) return r;
     }
     return LORA_OK;
   }
-  // The decode-path kernels (latency-bound, few bytes) run on a side stream
+  // The decode-path kernel (latency-bound, few bytes) runs on a side stream
   // while the tensor-path kernels (bandwidth-bound) run on the caller's
   // stream; the two touch disjoint rows of y and share only the metadata the
   // segment builder wrote before this call.  Fork and join are events, so the
@@ -196,10 +194,9 @@ int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, co
   int r = cuda_status(cudaEventRecord(side->fork, st), "cudaEventRecord(fork)");
   if (r == LORA_OK) r = cuda_status(cudaStreamWaitEvent(side->stream, side->fork, 0), "cudaStreamWaitEvent(fork)");
   if (r != LORA_OK) return r;
-  int rd = apply_stage(pool, seg, x, y, ldx, ldy, 1, side->stream);
-  if (rd == LORA_OK) rd = apply_stage(pool, seg, x, y, ldx, ldy, 2, side->stream);
-  int rt = apply_stage(pool, seg, x, y, ldx, ldy, 3, st);
-  if (rt == LORA_OK) rt = apply_stage(pool, seg, x, y, ldx, ldy, 4, st);
+  const int rd = run_stage(v, seg, x, y, ldx, ldy, 1, side->stream);
+  int rt = run_stage(v, seg, x, y, ldx, ldy, 2, st);
+  if (rt == LORA_OK) rt = run_stage(v, seg, x, y, ldx, ldy, 3, st);
   // join even after a failed launch, so the caller's stream never runs ahead
   r = cuda_status(cudaEventRecord(side->join, side->stream), "cudaEventRecord(join)");
   if (r == LORA_OK) r = cuda_status(cudaStreamWaitEvent(st, side->join, 0), "cudaStreamWaitEvent(join)");
@@ -212,9 +209,9 @@ int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void
                      int64_t ldy, int stage, lora_stream_t stream) {
   const int chk = check_apply(pool, seg, x, y, ldx, ldy);
   if (chk != LORA_OK) return chk;
-  if (stage < 1 || stage > 4) return LORA_ERR_ARG;
-  if (seg->T == 0 || !any_loaded(pool)) return LORA_OK;
-  return apply_stage(pool, seg, x, y, ldx, ldy, stage, reinterpret_cast<cudaStream_t>(stream));
+  if (stage < 1 || stage > 3) return LORA_ERR_ARG;
+  if (seg->T == 0 || !pool_has_adapter(pool)) return LORA_OK;
+  return run_stage(pool->v, seg, x, y, ldx, ldy, stage, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* lora_status_string(int status) {

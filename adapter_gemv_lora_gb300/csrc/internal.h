@@ -15,8 +15,6 @@ namespace lora {
 
 // Decode path tiling.
 constexpr int kDecGroup = LORA_DEC_GROUP_ROWS;  // rows of one slot per decode group
-constexpr int kDecKChunk = 1024;                // d_in elements per shrink item
-constexpr int kDecNChunk = 1024;                // output columns per expand item
 
 // Tensor path tiling.
 constexpr int kTcTile = LORA_TC_TILE_ROWS;  // MMA M
@@ -28,10 +26,6 @@ constexpr int kTcKSplit = 2;                // shrink K ranges per tile (fixed: 
 
 inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
 inline int ceil_div(int v, int m) { return (v + m - 1) / m; }
-
-struct TmapLanes {
-  CUtensorMap m[LORA_MAX_LANES];
-};
 
 // Tensor maps of one operand per lane in four box sizes: index s has a box of
 // 16 << s rank rows (A) or 1 << s groups of 16 rank columns (B), so a rank is
@@ -47,28 +41,40 @@ struct TmapSized {
 
 }  // namespace lora
 
-struct lora_pool {
+namespace lora {
+
+// Everything the kernels' launchers read from a pool, as plain data: the
+// shape, the factor regions, the tables, the tensor maps and the tensor
+// path's scratch.  An apply that runs on another scratch region copies the
+// view and replaces the three scratch pointers (and max_tokens, which sizes
+// the scratch), so the two can never read different fields.
+struct PoolView {
   int device = 0;
-  int N = 0, R = 0, R16 = 0, d_in = 0, L = 0, D = 0, max_tokens = 0, C_dec = 0;
+  int N = 0, R = 0, R16 = 0, d_in = 0, L = 0, D = 0, max_tokens = 0;
   int d_out[LORA_MAX_LANES] = {0, 0, 0, 0};
   int off[LORA_MAX_LANES] = {0, 0, 0, 0};
   char* base = nullptr;
   size_t bytes = 0;
-  int32_t* rank_tab = nullptr;      // [N][L]
-  float* scale_tab = nullptr;       // [N][L]
+  int32_t* rank_tab = nullptr;        // [N][L]
+  float* scale_tab = nullptr;         // [N][L]
   uint16_t* A[LORA_MAX_LANES] = {};   // per lane [N][R16][d_in]
   uint16_t* Bt[LORA_MAX_LANES] = {};  // per lane [N][R16][d_out]   (decode expand)
   uint16_t* Bk[LORA_MAX_LANES] = {};  // per lane [N][R16/16][d_out][16] (tensor expand: K-major
                                       // groups of 16 rank columns, each group contiguous)
-  float* u_dec = nullptr;           // [C_dec][max_tokens][L][R16] split-K partial sums
-  float* u_tc = nullptr;            // [kTcKSplit][tc_tile_cap][L][R16/4][128] float4 partial sums over K ranges
-  uint16_t* u_fmt = nullptr;        // [tc_tile_cap][L][2][128*R16] per tensor tile: U as bf16 hi then lo,
-                                    // K-major core-matrix layout of the tile's own rank, ready for the expand
-  int32_t* tile_cnt = nullptr;      // [tc_tile_cap] K-range CTAs of a tile that finished (0 between calls)
-  int32_t* dec_sched = nullptr;     // [4] decode shrink's item and finished-CTA counters (0 between calls)
-  std::vector<int> h_rank;          // host mirror of rank_tab
-  lora::TmapSized tm_a;             // A, 3-D {d_in, R16, N}, box {64, 16<<s, 1}, 128-byte swizzle
-  lora::TmapSized tm_bk;            // Bk, 3-D {16, d_out, R16/16*N}, box {16, 128, 1<<s}, 32-byte swizzle
+  // tensor-path scratch (tiles = tc_tile_cap(max_tokens))
+  float* u_tc = nullptr;              // [kTcKSplit][tiles][L][R16/4][128] float4 partial sums over K ranges
+  uint16_t* u_fmt = nullptr;          // [tiles][L][2][128*R16] per tensor tile: U as bf16 hi then lo,
+                                      // K-major core-matrix layout of the tile's own rank, ready for the expand
+  int32_t* tile_cnt = nullptr;        // [tiles] K-range CTAs of a tile that finished (0 between calls)
+  TmapSized tm_a;                     // A, 3-D {d_in, R16, N}, box {64, 16<<s, 1}, 128-byte swizzle
+  TmapSized tm_bk;                    // Bk, 3-D {16, d_out, R16/16*N}, box {16, 128, 1<<s}, 32-byte swizzle
+};
+
+}  // namespace lora
+
+struct lora_pool {
+  lora::PoolView v;
+  std::vector<int> h_rank;  // host mirror of rank_tab
 };
 
 struct lora_segments {
@@ -101,13 +107,25 @@ bool set_smem_limit(const void* kernel, int device, int bytes);
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* addr, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
 
+// Host-side checks of an apply call: pointers, alignment, leading dimensions,
+// shapes, and that the current device is the pool's and the segments' device.
+int check_apply(const lora_pool* pool, const lora_segments* seg, const void* x, const float* y, int64_t ldx,
+                int64_t ldy);
+
+// True if some (slot, lane) of the pool holds an adapter (host mirror).
+bool pool_has_adapter(const lora_pool* pool);
+// One kernel of the apply: 1 = decode (fused shrink -> expand), 2 = tensor
+// shrink, 3 = tensor expand.
+int run_stage(const PoolView& pool, const lora_segments* seg, const void* x, float* y, int64_t ldx, int64_t ldy,
+              int stage, cudaStream_t st);
+
 // The apply's side stream for the current device, created on first use.
 bool ensure_side_stream();
 
 // Launchers (return a LORA_* status).
 int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens, int S, int T,
                      cudaStream_t st);
-int launch_repack(lora_pool* pool, int slot, int lane, int rank, float scale, const uint16_t* A,
+int launch_repack(const PoolView& pool, int slot, int lane, int rank, float scale, const uint16_t* A,
                   const uint16_t* B, cudaStream_t st);
 // Launch `kernel` allowing programmatic dependent launch on `st` (the kernel
 // itself waits for its predecessor's results with griddepcontrol.wait).
@@ -127,13 +145,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-int launch_dec_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
-                      cudaStream_t st);
-int launch_dec_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy,
-                      cudaStream_t st);
-int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+// The decode path: one fused shrink -> expand kernel (u stays on chip).
+int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx, float* y,
+                  int64_t ldy, cudaStream_t st);
+int launch_tc_shrink(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
                      cudaStream_t st);
-int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy,
-                     cudaStream_t st);
+int launch_tc_expand(const PoolView& pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st);
 
 }  // namespace lora

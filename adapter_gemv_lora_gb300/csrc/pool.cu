@@ -15,7 +15,6 @@
 //                                       groups of 16 rank columns (K-major), so
 //                                       one TMA box loads several whole groups
 //                                       for the tensor-core expand
-//   u_dec     f32   [C][max_tokens][L][R16]  decode split-K partial sums
 //   u_tc      f32   [2][tiles][L][R16*128]   tensor-path partial sums, one per
 //                                            half of d_in, per tile as
 //                                            [column quad][row] float4
@@ -23,7 +22,7 @@
 //                                            bf16 hi and lo halves, in the
 //                                            layout the expand's MMA reads
 //   tile_cnt  int32 [tiles]                  per tile, K-range CTAs done
-//   dec_sched int32 [4]                      decode kernels' work-item counters
+// The decode path needs no scratch: its rank-space vector stays on chip.
 // (tiles = max_tokens / 64 + 1, the most a build can make)
 #include <cuda_runtime.h>
 
@@ -62,23 +61,21 @@ __global__ void repack_kernel(const uint16_t* __restrict__ A, const uint16_t* __
 }
 
 struct PoolLayout {
-  size_t rank_tab, scale_tab, A[LORA_MAX_LANES], Bt[LORA_MAX_LANES], Bk[LORA_MAX_LANES], u_dec, u_tc, u_fmt, tile_cnt,
-      dec_sched, total;
-  int R16, C_dec;
+  size_t rank_tab, scale_tab, A[LORA_MAX_LANES], Bt[LORA_MAX_LANES], Bk[LORA_MAX_LANES], u_tc, u_fmt, tile_cnt, total;
+  int R16;
 };
 
 size_t align1k(size_t v) { return (v + 1023) & ~(size_t)1023; }
 
 bool pool_layout(int N, int R, int d_in, int L, const int* d_out, int max_tokens, PoolLayout* P) {
-  if (N < 2 || N > LORA_MAX_SLOTS || R < 1 || R > 128 || d_in < 64 || (d_in % 64) || L < 1 || L > LORA_MAX_LANES ||
+  if (N < 2 || N > LORA_MAX_SLOTS || R < 1 || R > 128 || d_in < 64 || d_in > 65536 || (d_in % 64) || L < 1 ||
+      L > LORA_MAX_LANES ||
       !d_out || max_tokens < 1)
     return false;
-  const int R16 = round_up(R, 16);
-  if (L * R16 > 256) return false;
+  const int R16 = round_up(R, 16);  // L * R16 <= 4 * 128 = 512 TMEM columns for the tensor shrink
   for (int l = 0; l < L; ++l)
     if (d_out[l] < 64 || (d_out[l] % 64)) return false;
   P->R16 = R16;
-  P->C_dec = ceil_div(d_in, kDecKChunk);
   size_t o = 0;
   P->rank_tab = o; o = align1k(o + 4 * (size_t)N * L);
   P->scale_tab = o; o = align1k(o + 4 * (size_t)N * L);
@@ -92,29 +89,27 @@ bool pool_layout(int N, int R, int d_in, int L, const int* d_out, int max_tokens
   for (int l = 0; l < L; ++l) {
     P->Bk[l] = o; o = align1k(o + 2 * (size_t)N * d_out[l] * R16);
   }
-  P->u_dec = o; o = align1k(o + 4 * (size_t)P->C_dec * max_tokens * L * R16);
   P->u_tc = o; o = align1k(o + 4 * (size_t)kTcKSplit * tc_tile_cap(max_tokens) * L * R16 * kTcTile);
   P->u_fmt = o; o = align1k(o + 2 * (size_t)tc_tile_cap(max_tokens) * L * 2 * kTcTile * R16);
   P->tile_cnt = o; o = align1k(o + 4 * (size_t)tc_tile_cap(max_tokens));
-  P->dec_sched = o; o = align1k(o + 4 * 4);
   P->total = o;
   return true;
 }
 
 }  // namespace
 
-int launch_repack(lora_pool* pool, int slot, int lane, int rank, float scale, const uint16_t* A, const uint16_t* B,
-                  cudaStream_t st) {
-  const int R16 = pool->R16, d_in = pool->d_in, d_out = pool->d_out[lane];
-  uint16_t* Ap = pool->A[lane] + (size_t)slot * R16 * d_in;
-  uint16_t* Bt = pool->Bt[lane] + (size_t)slot * R16 * d_out;
-  uint16_t* Bk = pool->Bk[lane] + (size_t)slot * d_out * R16;
+int launch_repack(const PoolView& pool, int slot, int lane, int rank, float scale, const uint16_t* A,
+                  const uint16_t* B, cudaStream_t st) {
+  const int R16 = pool.R16, d_in = pool.d_in, d_out = pool.d_out[lane];
+  uint16_t* Ap = pool.A[lane] + (size_t)slot * R16 * d_in;
+  uint16_t* Bt = pool.Bt[lane] + (size_t)slot * R16 * d_out;
+  uint16_t* Bk = pool.Bk[lane] + (size_t)slot * d_out * R16;
   const size_t n = (size_t)R16 * (d_in > d_out ? d_in : d_out);
   int blocks = (int)((n + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   repack_kernel<<<blocks, 256, 0, st>>>(A, B, rank, R16, d_in, d_out, Ap, Bt, Bk,
-                                         pool->rank_tab + slot * pool->L + lane,
-                                         pool->scale_tab + slot * pool->L + lane, scale);
+                                         pool.rank_tab + slot * pool.L + lane, pool.scale_tab + slot * pool.L + lane,
+                                         scale);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError(), "repack_kernel launch");
 }
@@ -138,9 +133,10 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   if (!pool_layout(num_slots, max_rank, d_in, num_lanes, lane_d_out, max_tokens, &P)) return LORA_ERR_SHAPE;
   if (bytes < P.total) return LORA_ERR_SHAPE;
   ensure_side_stream();  // now, not inside a caller's stream capture (the apply works without it)
-  lora_pool* p = new lora_pool();
+  lora_pool* pp = new lora_pool();
+  PoolView* p = &pp->v;
   if (cudaGetDevice(&p->device) != cudaSuccess) {
-    delete p;
+    delete pp;
     return LORA_ERR_CUDA;
   }
   char* b = static_cast<char*>(dev_mem);
@@ -150,7 +146,6 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   p->d_in = d_in;
   p->L = num_lanes;
   p->max_tokens = max_tokens;
-  p->C_dec = P.C_dec;
   p->base = b;
   p->bytes = bytes;
   p->D = 0;
@@ -164,12 +159,10 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   }
   p->rank_tab = reinterpret_cast<int32_t*>(b + P.rank_tab);
   p->scale_tab = reinterpret_cast<float*>(b + P.scale_tab);
-  p->u_dec = reinterpret_cast<float*>(b + P.u_dec);
   p->u_tc = reinterpret_cast<float*>(b + P.u_tc);
   p->u_fmt = reinterpret_cast<uint16_t*>(b + P.u_fmt);
   p->tile_cnt = reinterpret_cast<int32_t*>(b + P.tile_cnt);
-  p->dec_sched = reinterpret_cast<int32_t*>(b + P.dec_sched);
-  p->h_rank.assign((size_t)num_slots * num_lanes, 0);
+  pp->h_rank.assign((size_t)num_slots * num_lanes, 0);
   std::memset(&p->tm_a, 0, sizeof(p->tm_a));
   std::memset(&p->tm_bk, 0, sizeof(p->tm_bk));
   for (int l = 0; l < num_lanes; ++l) {
@@ -181,7 +174,7 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
         const uint32_t box[3] = {(uint32_t)kTcKBlock, 16u << sz, 1u};
         if (!encode_tmap(&p->tm_a.m[sz][l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->A[l], dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_128B)) {
-          delete p;
+          delete pp;
           return LORA_ERR_CUDA;
         }
       }
@@ -191,35 +184,35 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
         const uint32_t box[3] = {16u, (uint32_t)kTcNT, 1u << sz};
         if (!encode_tmap(&p->tm_bk.m[sz][l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->Bk[l], dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_32B)) {
-          delete p;
+          delete pp;
           return LORA_ERR_CUDA;
         }
       }
     }
   }
   if (cudaMemsetAsync(dev_mem, 0, P.total, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    delete p;
+    delete pp;
     return LORA_ERR_CUDA;
   }
-  *out = p;
+  *out = pp;
   return LORA_OK;
 }
 
 int lora_pool_load(lora_pool* pool, int slot, int lane, int rank, float scale, const void* A, const void* B,
                    lora_stream_t stream) {
   if (!pool) return LORA_ERR_ARG;
-  if (slot < 1 || slot >= pool->N) return LORA_ERR_SLOT;
-  if (lane < 0 || lane >= pool->L) return LORA_ERR_ARG;
-  if (rank < 0 || rank > pool->R) return LORA_ERR_RANK;
+  const PoolView& v = pool->v;
+  if (slot < 1 || slot >= v.N) return LORA_ERR_SLOT;
+  if (lane < 0 || lane >= v.L) return LORA_ERR_ARG;
+  if (rank < 0 || rank > v.R) return LORA_ERR_RANK;
   if (rank > 0 && (!A || !B)) return LORA_ERR_ARG;
   if (rank > 0 && (reinterpret_cast<uintptr_t>(A) & 1 || reinterpret_cast<uintptr_t>(B) & 1)) return LORA_ERR_ARG;
   int dev = -1;  // the repack runs on the current device, where the pool must live
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
-  if (dev != pool->device) return LORA_ERR_ARG;
-  const int st = launch_repack(pool, slot, lane, rank, rank > 0 ? scale : 0.0f,
-                               static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B),
-                               reinterpret_cast<cudaStream_t>(stream));
-  if (st == LORA_OK) pool->h_rank[(size_t)slot * pool->L + lane] = rank;
+  if (dev != v.device) return LORA_ERR_ARG;
+  const int st = launch_repack(v, slot, lane, rank, rank > 0 ? scale : 0.0f, static_cast<const uint16_t*>(A),
+                               static_cast<const uint16_t*>(B), reinterpret_cast<cudaStream_t>(stream));
+  if (st == LORA_OK) pool->h_rank[(size_t)slot * v.L + lane] = rank;
   return st;
 }
 

@@ -620,13 +620,13 @@ int tc_tile_bound(const lora_segments* seg) {
 
 }  // namespace
 
-int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+int launch_tc_shrink(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
                      cudaStream_t st) {
   const int grid = tc_tile_bound(seg) * kTcKSplit;
   if (grid <= 0) return LORA_OK;
   CUtensorMap tm_x128, tm_x32;
   {
-    const uint64_t dims[2] = {(uint64_t)pool->d_in, (uint64_t)seg->T};
+    const uint64_t dims[2] = {(uint64_t)pool.d_in, (uint64_t)seg->T};
     const uint64_t strides[1] = {2ull * (uint64_t)ldx};
     const uint32_t box128[2] = {(uint32_t)kTcKBlock, (uint32_t)kTcTile};
     const uint32_t box32[2] = {(uint32_t)kTcKBlock, (uint32_t)kXBoxRows};
@@ -639,56 +639,60 @@ int launch_tc_shrink(const lora_pool* pool, const lora_segments* seg, const uint
   TcShrinkParams p{};
   p.counts = seg->counts;
   p.work = seg->tc_work;
-  p.rank_tab = pool->rank_tab;
-  p.u_tc = pool->u_tc;
-  p.u_fmt = pool->u_fmt;
-  p.tile_cnt = pool->tile_cnt;
+  p.rank_tab = pool.rank_tab;
+  p.u_tc = pool.u_tc;
+  p.u_fmt = pool.u_fmt;
+  p.tile_cnt = pool.tile_cnt;
   p.status = seg->status;
-  p.L = pool->L;
-  p.R16 = pool->R16;
-  p.num_kb = pool->d_in / kTcKBlock;
-  p.tiles_cap = tc_tile_cap(pool->max_tokens);
-  p.u_split_stride = (size_t)p.tiles_cap * pool->L * pool->R16 * kTcTile;
+  p.L = pool.L;
+  p.R16 = pool.R16;
+  p.num_kb = pool.d_in / kTcKBlock;
+  p.tiles_cap = tc_tile_cap(pool.max_tokens);
+  p.u_split_stride = (size_t)p.tiles_cap * pool.L * pool.R16 * kTcTile;
   // Two CTAs per SM: each keeps its ring within ~100 KB of shared memory (at
   // least two stages of the largest kind: every lane at R16).
-  const int max_stage = kXStageBytes + pool->L * pool->R16 * kTcKBlock * 2;
+  const int max_stage = kXStageBytes + pool.L * pool.R16 * kTcKBlock * 2;
   p.ring_bytes = 100 * 1024 > 2 * max_stage ? 100 * 1024 : 2 * max_stage;
   int cols = 32;
-  while (cols < pool->L * pool->R16) cols <<= 1;
+  while (cols < pool.L * pool.R16) cols <<= 1;
   p.tmem_cols = cols;
+  // Above 256 TMEM columns a CTA needs more than half of the SM's 512: ask for
+  // enough shared memory that only one CTA fits on an SM, so no CTA's
+  // allocation waits for another's to be released.
+  if (cols > 256 && p.ring_bytes < 120 * 1024) p.ring_bytes = 120 * 1024;
   const int smem = p.ring_bytes + 1024;
-  if (!set_smem_limit(reinterpret_cast<const void*>(tc_shrink_kernel), pool->device, smem)) return LORA_ERR_CUDA;
-  const cudaError_t e = launch_pdl(tc_shrink_kernel, dim3(grid), dim3(kTcThreads), smem, st, tm_x128, tm_x32, pool->tm_a, p);
+  if (!set_smem_limit(reinterpret_cast<const void*>(tc_shrink_kernel), pool.device, smem)) return LORA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(tc_shrink_kernel, dim3(grid), dim3(kTcThreads), smem, st, tm_x128, tm_x32, pool.tm_a, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "tc_shrink_kernel launch");
 }
 
-int launch_tc_expand(const lora_pool* pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {
+int launch_tc_expand(const PoolView& pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {
   TcExpandParams p{};
   p.ng_base[0] = 0;
   for (int l = 0; l < LORA_MAX_LANES; ++l) {
-    p.d_out[l] = pool->d_out[l];
-    p.off[l] = pool->off[l];
-    p.ng_base[l + 1] = p.ng_base[l] + (l < pool->L ? ceil_div(pool->d_out[l], kTcNGroup) : 0);
+    p.d_out[l] = pool.d_out[l];
+    p.off[l] = pool.off[l];
+    p.ng_base[l + 1] = p.ng_base[l] + (l < pool.L ? ceil_div(pool.d_out[l], kTcNGroup) : 0);
   }
-  p.total_ng = p.ng_base[pool->L];
-  p.tail_items = sm_count(pool->device) / 2;  // half an SM wave: measured best of 0.5, 1 and 2 waves
+  p.total_ng = p.ng_base[pool.L];
+  p.tail_items = sm_count(pool.device) / 2;  // half an SM wave: measured best of 0.5, 1 and 2 waves
   const long long items = (long long)tc_tile_bound(seg) * p.total_ng;
   if (items <= 0) return LORA_OK;
   const long long grid = items + p.tail_items;  // the tail's items take two CTAs each
   p.counts = seg->counts;
   p.work = seg->tc_work;
-  p.rank_tab = pool->rank_tab;
-  p.scale_tab = pool->scale_tab;
-  p.u_fmt = pool->u_fmt;
+  p.rank_tab = pool.rank_tab;
+  p.scale_tab = pool.scale_tab;
+  p.u_fmt = pool.u_fmt;
   p.y = y;
   p.ldy = ldy;
   p.status = seg->status;
-  p.L = pool->L;
-  p.R16 = pool->R16;
-  const int smem = 2 * kHalfBytes + 4 * kTcTile * pool->R16 * 2 + 1024;  // staging + 2 B stages + U hi/lo
-  if (!set_smem_limit(reinterpret_cast<const void*>(tc_expand_kernel), pool->device, smem)) return LORA_ERR_CUDA;
-  const cudaError_t e = launch_pdl(tc_expand_kernel, dim3((unsigned)grid), dim3(kExpThreads), smem, st, pool->tm_bk, p);
+  p.L = pool.L;
+  p.R16 = pool.R16;
+  const int smem = 2 * kHalfBytes + 4 * kTcTile * pool.R16 * 2 + 1024;  // staging + 2 B stages + U hi/lo
+  if (!set_smem_limit(reinterpret_cast<const void*>(tc_expand_kernel), pool.device, smem)) return LORA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(tc_expand_kernel, dim3((unsigned)grid), dim3(kExpThreads), smem, st, pool.tm_bk, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "tc_expand_kernel launch");
 }

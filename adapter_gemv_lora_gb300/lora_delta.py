@@ -308,5 +308,6 @@ def apply(pool: LoraPool, seg: LoraSegments, x, y, stream=None) -> None:
 
 
 def apply_stage(pool: LoraPool, seg: LoraSegments, x, y, stage: int, stream=None) -> None:
+    """One kernel of apply(): 1 = decode path (fused shrink -> expand), 2 = tensor shrink, 3 = tensor expand."""
     lora_apply_stage(pool.handle, seg.handle, x.data_ptr(), y.data_ptr(), x.stride(0), y.stride(0), stage,
                      _stream(stream))

@@ -2,16 +2,19 @@
 """Benchmark of the mixed-adapter LoRA delta on one GB300 (or N replicas).
 
 One step = one pass of the whole hot path over one batch: lora_build_segments
-(routing metadata) followed, for every projection of the workload, by the four
-kernels of lora_apply_shrink_expand (decode shrink, decode expand, tensor
-shrink, tensor expand).  Inputs are resident in HBM before timing starts.
-Between timed steps y is restored and L2 is flushed (a 256 MiB write), both
-outside the CUDA events that time the step.
+(routing metadata) followed, for every projection of the workload, by the
+kernels of lora_apply_shrink_expand (the fused decode kernel, the tensor
+shrink and the tensor expand).  Inputs are resident in HBM before timing
+starts.  Between timed steps y is restored and L2 is flushed (a 256 MiB
+write), both outside the CUDA events that time the step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
-on its own GPU (no data exchange; weak scaling); times are max-reduced.
+Prints one JSON line (rank 0): the headline workload (cont_batch by default)
+and, under "per_workload", every configuration with its step, apply-only and
+segment-build times, per-kernel times, roofline fractions and the oracle's
+single-thread and all-core rates.  Under torchrun every rank runs its own
+batch on its own GPU (no data exchange; weak scaling); times are max-reduced.
 """
 from __future__ import annotations
 
@@ -34,9 +37,10 @@ from adapter_gemv_lora_gb300 import workloads as W  # noqa: E402
 
 METRIC = "LoRA-delta tokens/s; HBM GB/s (decode) & TFLOP/s (prefill) as % roofline"
 TC_MIN_QLEN = 64  # documented tensor-path threshold of the library (own sequence length)
-STAGES = ["dec_shrink", "dec_expand", "tc_shrink", "tc_expand"]
-KERNEL_NAMES = {"dec_shrink": "dec_shrink_kernel", "dec_expand": "dec_expand_kernel",
-                "tc_shrink": "tc_shrink_kernel", "tc_expand": "tc_expand_kernel", "seg_build": "seg_build_kernel"}
+STAGES = ["decode", "tc_shrink", "tc_expand"]  # lora_apply_stage 1, 2, 3
+KERNEL_NAMES = {"decode": "dec_fused_kernel", "tc_shrink": "tc_shrink_kernel", "tc_expand": "tc_expand_kernel",
+                "seg_build": "seg_build_kernel"}
+KERNEL_SOURCES = {"decode": "decode.cu", "tc_shrink": "tensor.cu", "tc_expand": "tensor.cu"}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -61,38 +65,60 @@ def measured_peaks():
 def algorithmic_units(wl: W.Workload):
     """Per projection and per kernel: algorithmic bytes and flops of one step.
 
-    Per active row: 2*d_in bytes of x (shrink) and 8*D bytes of y (fp32 read +
-    write, expand).  Per (slot, lane) present on a path: 2*r*d_in bytes of A
-    (shrink) and 2*r*d_out bytes of B (expand), true rank only.  Base rows and
-    rank-0 lanes cost nothing.  flops = sum over active rows and loaded lanes
-    of 2*r*(d_in + d_out)."""
+    Per active row: 2*d_in bytes of x and 8*D bytes of y (fp32 read + write;
+    the decode kernel moves both, the tensor shrink x and the tensor expand
+    y).  Per (slot, lane) present on a kernel's rows: 2*r*d_in bytes of A
+    (decode kernel, tensor shrink) and 2*r*d_out bytes of B (decode kernel,
+    tensor expand), true rank only; a slot with rows on both paths is read by
+    both paths' kernels, so each kernel counts its own factor reads.  Base
+    rows and rank-0 lanes cost nothing.  flops = sum over active rows and
+    loaded lanes of 2*r*(d_in + d_out)."""
     slot = np.repeat(wl.adapter_ids, wl.q_seq_lens)
     qlen = np.repeat(wl.q_seq_lens, wl.q_seq_lens)
     cls = (qlen >= TC_MIN_QLEN).astype(np.int64)
     out = []
     for proj in wl.projections:
         u = {s: {"bytes": 0, "flops": 0, "rows": 0} for s in STAGES}
-        for c, (sh, ex) in enumerate([("dec_shrink", "dec_expand"), ("tc_shrink", "tc_expand")]):
+        for c in (0, 1):
             rows = (slot != 0) & (cls == c)
             ks = slot[rows]
+            sh, ex = ("decode", "decode") if c == 0 else ("tc_shrink", "tc_expand")
             for k in np.unique(ks):
                 n = int((ks == k).sum())
-                for l, dout in enumerate(proj.lane_d_out):
-                    r = int(proj.rank[k, l])
-                    if r <= 0:
-                        continue
-                    u[sh]["bytes"] += 2 * r * proj.d_in
-                    u[ex]["bytes"] += 2 * r * dout
-                    u[sh]["flops"] += n * 2 * r * proj.d_in
-                    u[ex]["flops"] += n * 2 * r * dout
                 loaded = [l for l in range(proj.num_lanes) if proj.rank[k, l] > 0]
+                for l in loaded:
+                    r = int(proj.rank[k, l])
+                    u[sh]["bytes"] += 2 * r * proj.d_in
+                    u[ex]["bytes"] += 2 * r * proj.lane_d_out[l]
+                    u[sh]["flops"] += n * 2 * r * proj.d_in
+                    u[ex]["flops"] += n * 2 * r * proj.lane_d_out[l]
                 if loaded:
                     u[sh]["bytes"] += n * 2 * proj.d_in
                     u[ex]["bytes"] += n * 8 * sum(proj.lane_d_out[l] for l in loaded)
                     u[sh]["rows"] += n
-                    u[ex]["rows"] += n
+                    if ex != sh:
+                        u[ex]["rows"] += n
         out.append(u)
     return out
+
+
+def step_bytes(wl: W.Workload):
+    """Algorithmic bytes and flops of the whole step: every active row's x and
+    y once, and every present (slot, lane)'s factors once, whichever paths its
+    rows take."""
+    slot = np.repeat(wl.adapter_ids, wl.q_seq_lens)
+    total, flops = 0, 0
+    for proj in wl.projections:
+        for k in np.unique(slot[slot != 0]):
+            n = int((slot == k).sum())
+            loaded = [l for l in range(proj.num_lanes) if proj.rank[k, l] > 0]
+            for l in loaded:
+                r = int(proj.rank[k, l])
+                total += 2 * r * (proj.d_in + proj.lane_d_out[l])
+                flops += n * 2 * r * (proj.d_in + proj.lane_d_out[l])
+            if loaded:
+                total += n * (2 * proj.d_in + 8 * sum(proj.lane_d_out[l] for l in loaded))
+    return total, flops
 
 
 class ClockSampler:
@@ -158,7 +184,8 @@ def traffic_from_profile(kernel: str, workload: str):
             k, v = ln.split(":", 1)
             vals[k.strip()] = v.strip()
     src = os.path.join(ROOT, "adapter_gemv_lora_gb300", "csrc",
-                       "tensor.cu" if kernel.startswith("tc_") else "decode.cu")
+                       "tensor.cu" if kernel.startswith("tc_") else
+                       "segments.cu" if kernel.startswith("seg_") else "decode.cu")
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     if vals.get("source_sha256_16") != sha:
         return None
@@ -208,116 +235,136 @@ def setup_device_workload(wl, dev):
 
 
 def time_ours(wl, steps, warmup, dev, sampler_index):
+    """Device times of one workload's step.
+
+    * eager pass: CUDA events between every kernel (lora_apply_stage) on the
+      launching stream -> per-kernel and segment-build times;
+    * the step as a serving engine runs it (lora_build_segments +
+      lora_apply_shrink_expand per projection) captured once in a CUDA graph
+      and replayed -> step time (the headline), checked bit for bit against
+      an eager step;
+    * the applies alone (segments built once before) and the build alone,
+      each captured and replayed the same way -> apply-only and build times.
+    y is restored and L2 flushed before every timed replay, outside the events."""
     import torch
     from adapter_gemv_lora_gb300 import lora_delta as LD
     projs, seg, ids, lens = setup_device_workload(wl, dev)
     T = wl.T
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    n_ev = 2 + 4 * len(projs)
-
-    def one_step(evs):
-        evs[0].record(stream)
-        seg.build(ids, lens, num_tokens=T)
-        evs[1].record(stream)
-        i = 2
-        for pr in projs:
-            for stage in range(1, 5):
-                LD.apply_stage(pr["pool"], seg, pr["x"], pr["y"], stage)
-                evs[i].record(stream)
-                i += 1
+    n_ev = 2 + len(STAGES) * len(projs)
 
     def reset():
         for pr in projs:
             pr["y"].copy_(pr["y0"])
         flush.fill_(1)
 
+    def build():
+        LD.lora_build_segments(seg.handle, ids.data_ptr(), lens.data_ptr(), wl.S, T,
+                               torch.cuda.current_stream().cuda_stream)
+
+    def applies():
+        for pr in projs:
+            LD.apply(pr["pool"], seg, pr["x"], pr["y"])
+
+    def public_step():
+        build()
+        applies()
+
+    def one_eager(evs):
+        evs[0].record(stream)
+        build()
+        evs[1].record(stream)
+        i = 2
+        for pr in projs:
+            for stage in range(1, len(STAGES) + 1):
+                LD.apply_stage(pr["pool"], seg, pr["x"], pr["y"], stage)
+                evs[i].record(stream)
+                i += 1
+
     evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
     warm = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     for _ in range(warmup):
         reset()
-        one_step(warm)
+        one_eager(warm)
     torch.cuda.synchronize()
     assert seg.status() == 0, LD.lora_status_string(seg.status())
-    sampler = ClockSampler(sampler_index)
-    with sampler:
-        time.sleep(0.3)
-        barrier()
-        torch.cuda.synchronize()
-        n0 = LD.lora_launch_count()
-        for s in range(steps):
-            reset()
-            one_step(evsets[s])
-        n1 = LD.lora_launch_count()
-        torch.cuda.synchronize()
-        barrier()
+    barrier()
+    torch.cuda.synchronize()
+    n0 = LD.lora_launch_count()
+    for st in range(steps):
+        reset()
+        one_eager(evsets[st])
+    n1 = LD.lora_launch_count()
+    torch.cuda.synchronize()
+    barrier()
     assert seg.status() == 0, LD.lora_status_string(seg.status())
-    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in evsets]
-    seg_ms = [ev[0].elapsed_time(ev[1]) for ev in evsets]
     stage_ms = []
     for p in range(len(projs)):
         per = {}
         for j, name in enumerate(STAGES):
-            a, b = 1 + 4 * p + j, 2 + 4 * p + j
+            a, b = 1 + len(STAGES) * p + j, 2 + len(STAGES) * p + j
             per[name] = statistics.mean(ev[a].elapsed_time(ev[b]) for ev in evsets)
         stage_ms.append(per)
-    res = {"step_ms_eager": statistics.mean(step_ms), "seg_ms": statistics.mean(seg_ms), "stage_ms": stage_ms,
-           "launches_eager": n1 - n0, "clocks_eager": sampler.summary()}
+    res = {"step_ms_eager": statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in evsets),
+           "seg_ms_eager": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evsets),
+           "stage_ms": stage_ms, "launches_eager": n1 - n0}
 
-    # The step as a serving engine runs it: lora_build_segments + lora_apply_shrink_expand
-    # per projection, captured once in a CUDA graph and replayed, so host launch
-    # latency is not counted.  The replay is checked bit for bit against an eager step.
-    def public_step():
-        LD.lora_build_segments(seg.handle, ids.data_ptr(), lens.data_ptr(), wl.S, T,
-                               torch.cuda.current_stream().cuda_stream)
-        for pr in projs:
-            LD.apply(pr["pool"], seg, pr["x"], pr["y"])
-
+    # reference bits: one eager public step from the restored inputs
     reset()
     public_step()
     torch.cuda.synchronize()
     y_eager = [pr["y"].clone() for pr in projs]
-    graph = None
-    try:
-        graph = torch.cuda.CUDAGraph()
+
+    def graph_loop(fn, check, sampled):
+        g = torch.cuda.CUDAGraph()
         n_cap0 = LD.lora_launch_count()
-        with torch.cuda.graph(graph):
-            public_step()
-        per_step_launches = LD.lora_launch_count() - n_cap0
-        reset()
-        graph.replay()
-        torch.cuda.synchronize()
-        for pr, ye in zip(projs, y_eager):
-            assert torch.equal(pr["y"].view(torch.int32), ye.view(torch.int32)), "graph replay differs from eager"
-    except Exception as e:  # capture not possible here: time eager public calls instead
-        print(f"graph capture unavailable ({e}); timing eager calls", file=sys.stderr)
-        graph = None
-        per_step_launches = None
-    for _ in range(warmup):
-        reset()
-        graph.replay() if graph is not None else public_step()
-    torch.cuda.synchronize()
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    sampler = ClockSampler(sampler_index)
-    with sampler:
-        time.sleep(0.3)
-        barrier()
-        torch.cuda.synchronize()
-        n0 = LD.lora_launch_count()
-        for s in range(steps):
+        with torch.cuda.graph(g):
+            fn()
+        per_replay = LD.lora_launch_count() - n_cap0
+        if check:
             reset()
-            gev[s][0].record(stream)
-            graph.replay() if graph is not None else public_step()
-            gev[s][1].record(stream)
-        n1 = LD.lora_launch_count()
+            g.replay()
+            torch.cuda.synchronize()
+            for pr, ye in zip(projs, y_eager):
+                assert torch.equal(pr["y"].view(torch.int32), ye.view(torch.int32)), "graph replay differs from eager"
+        for _ in range(warmup):
+            reset()
+            g.replay()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        sampler = ClockSampler(sampler_index) if sampled else None
+        if sampler:
+            # the clock samples cover sustained replays of this graph: about
+            # 0.6 s of untimed replays right before the timed ones
+            sampler.__enter__()
+            t_end = time.perf_counter() + 0.6
+            while time.perf_counter() < t_end:
+                for _ in range(20):
+                    reset()
+                    g.replay()
+                torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        for st in range(steps):
+            reset()
+            gev[st][0].record(stream)
+            g.replay()
+            gev[st][1].record(stream)
         torch.cuda.synchronize()
         barrier()
+        if sampler:
+            sampler.__exit__()
+        ms = [a.elapsed_time(b) for a, b in gev]
+        return ms, per_replay * steps, (sampler.summary() if sampler else None)
+
+    gms, launches, clocks = graph_loop(public_step, True, True)
+    ams, _, _ = graph_loop(applies, True, False)  # segments were built by the eager step above
+    sms, _, _ = graph_loop(build, False, False)
     assert seg.status() == 0, LD.lora_status_string(seg.status())
-    gms = [a.elapsed_time(b) for a, b in gev]
     res.update({"step_ms": statistics.mean(gms), "step_ms_median": statistics.median(gms),
-                "graph": graph is not None,
-                "launches": (per_step_launches * steps) if graph is not None else (n1 - n0),
-                "clocks": sampler.summary()})
+                "apply_ms": statistics.mean(ams), "seg_ms": statistics.mean(sms), "graph": True,
+                "launches": launches, "clocks": clocks})
     del flush
     return res, (projs, seg, ids, lens)
 
@@ -398,17 +445,22 @@ def time_e2e(wl, ctx, steps, warmup, dev):
     return ms, h2d, d2h
 
 
-def cpu_oracle_rate(wl, target_s: float, seed: int = 0):
-    """The oracle (as it is) on host cores over a random sample of the step's rows.
+def cpu_oracle_rates(wl, threads: int, target_s: float, runs: int = 3, seed: int = 0):
+    """The oracle (as it is) on `threads` host threads (0 = all cores).
 
-    Returns (rows/s, cores, sample description, seconds)."""
+    The metadata phase (single-threaded code) is timed on the whole step; the
+    delta phase on a seeded random sample of the step's rows, sized so that
+    one run takes about target_s.  Each phase is the median of `runs` runs.
+    tokens/s = T / (metadata time + T * delta time per row)."""
     import oracle
     oracle.build()
-    cores = oracle.max_threads()
+    cores = oracle.max_threads() if threads <= 0 else threads
     rng = np.random.default_rng(seed)
-    t0 = time.perf_counter()
-    meta = oracle.segments(wl.adapter_ids, wl.q_seq_lens, wl.T, wl.num_slots, TC_MIN_QLEN, 128, 8)
-    t_meta = time.perf_counter() - t0
+    meta_t = []
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        meta = oracle.segments(wl.adapter_ids, wl.q_seq_lens, wl.T, wl.num_slots, TC_MIN_QLEN, 128, 8)
+        meta_t.append(time.perf_counter() - t0)
     slot = meta["slot"]
     flats = [oracle.flatten_factors(p) for p in wl.projections]
 
@@ -416,17 +468,23 @@ def cpu_oracle_rate(wl, target_s: float, seed: int = 0):
         rows = np.sort(rng.choice(wl.T, size=n, replace=False))
         t = time.perf_counter()
         for p, fl in zip(wl.projections, flats):
-            oracle.delta(p, slot, rows=rows, _flat=fl)
+            oracle.delta(p, slot, rows=rows, num_threads=cores, _flat=fl)
         return time.perf_counter() - t
 
-    n = min(64, wl.T)
+    n = min(16, wl.T)
     dt = run(n)
-    while dt < 0.2 * target_s and n < wl.T:
-        n = min(wl.T, max(2 * n, int(n * target_s / max(dt, 1e-3) * 0.5)))
+    while dt < 0.3 * target_s and n < wl.T:
+        n = min(wl.T, max(2 * n, int(n * target_s / max(dt, 1e-4) * 0.8)))
         dt = run(n)
-    # the metadata of the whole step is part of the path; charge it per sampled row
-    dt_total = dt + t_meta * n / wl.T
-    return n / dt_total, cores, f"{n} of {wl.T} rows of one step (uniform random), fp64, {cores} threads", dt_total
+    delta_t = sorted(run(n) for _ in range(runs))[runs // 2]
+    meta_s = sorted(meta_t)[runs // 2]
+    per_row = delta_t / n
+    total = meta_s + wl.T * per_row
+    return {"tokens_per_s": round(wl.T / total, 2), "threads": cores, "meta_ms": round(1e3 * meta_s, 3),
+            "delta_us_per_row": round(1e6 * per_row, 3), "delta_rows_per_s": round(1.0 / per_row, 2),
+            "step_s": round(total, 4), "sample_rows": n, "runs": runs,
+            "sample": f"metadata on all {wl.T} rows; delta on {n} of {wl.T} rows (seeded uniform sample), "
+                      f"fp64, {cores} thread(s), median of {runs}"}
 
 
 def barrier():
@@ -445,6 +503,49 @@ def max_over_ranks(v: float) -> float:
     return v
 
 
+def workload_config(wl, ws):
+    """The config dict of a bench line (the same for both arms)."""
+    active = int((np.repeat(wl.adapter_ids, wl.q_seq_lens) != 0).sum())
+    return {"workload": wl.name, "tokens": wl.T, "active_tokens": active, "sequences": wl.S,
+            "slots": wl.num_slots,
+            "projections": [{"name": p.name, "d_in": p.d_in, "lanes": p.lane_d_out, "max_rank": p.max_rank}
+                            for p in wl.projections],
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+            "timing": "CUDA-graph replay of build_segments + apply per step (checked bit-exact against "
+                      "an eager step); per-kernel times from an eager pass with events between kernels",
+            "parallelism": f"replicas x{ws} (no exchange)"}
+
+
+def workload_record(wl, res, hbm_peak, bf16_peak):
+    """Times, algorithmic bytes and roofline fractions of one workload."""
+    units = algorithmic_units(wl)
+    kernels = {}
+    for p, (u, sm) in enumerate(zip(units, res["stage_ms"])):
+        for name in STAGES:
+            ms = sm[name]
+            b, f = u[name]["bytes"], u[name]["flops"]
+            key = name if len(units) == 1 else f"{wl.projections[p].name}.{name}"
+            kernels[key] = {"ms": round(ms, 5), "alg_bytes": int(b), "flops": int(f),
+                            "gbs": round(b / (ms * 1e-3) / 1e9, 1) if ms > 0 and b else 0.0,
+                            "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4) if ms > 0 and b else 0.0,
+                            "tflops": round(f / (ms * 1e-3) / 1e12, 2) if ms > 0 and f else 0.0}
+    sb, sf = step_bytes(wl)
+    step_ms, apply_ms = res["step_ms"], res["apply_ms"]
+    return {"tokens": wl.T, "active_tokens": int((np.repeat(wl.adapter_ids, wl.q_seq_lens) != 0).sum()),
+            "ms_per_step": round(step_ms, 5), "ms_per_step_median": round(res["step_ms_median"], 5),
+            "ms_per_step_eager": round(res["step_ms_eager"], 5),
+            "tokens_per_s": round(wl.T / (step_ms * 1e-3), 1),
+            "apply_ms": round(apply_ms, 5), "seg_build_ms": round(res["seg_ms"], 5),
+            "alg_bytes": int(sb), "flops": int(sf),
+            "gbs_step": round(sb / (step_ms * 1e-3) / 1e9, 1),
+            "frac_hbm_step": round(sb / (step_ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "gbs_apply": round(sb / (apply_ms * 1e-3) / 1e9, 1),
+            "frac_hbm_apply": round(sb / (apply_ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "tflops_apply": round(sf / (apply_ms * 1e-3) / 1e12, 2),
+            "frac_bf16_apply": round(sf / (apply_ms * 1e-3) / 1e12 / bf16_peak, 5),
+            "kernels": kernels}
+
+
 def run_ours(args):
     import torch
     ws, rank, local = dist_env()
@@ -461,42 +562,33 @@ def run_ours(args):
         wl = truncate_workload(wl, args.max_seqs)
     res, ctx = time_ours(wl, args.steps, args.warmup, dev, local)
     step_ms = max_over_ranks(res["step_ms"])
-    units = algorithmic_units(wl)
     hbm_peak, bf16_peak, peak_src = measured_peaks()
-    # per-kernel roofline
-    kernels = {}
-    for p, (u, sm) in enumerate(zip(units, res["stage_ms"])):
-        for name in STAGES:
-            ms = sm[name]
-            b, f = u[name]["bytes"], u[name]["flops"]
-            key = name if len(units) == 1 else f"{wl.projections[p].name}.{name}"
-            kernels[key] = {"ms": round(ms, 5), "alg_bytes": int(b), "flops": int(f),
-                            "gbs": round(b / (ms * 1e-3) / 1e9, 1) if ms > 0 and b else 0.0,
-                            "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4) if ms > 0 and b else 0.0,
-                            "tflops": round(f / (ms * 1e-3) / 1e12, 2) if ms > 0 and f else 0.0}
+    rec = workload_record(wl, res, hbm_peak, bf16_peak)
+    kernels = rec["kernels"]
     dom_key = max(kernels, key=lambda k: kernels[k]["ms"])
     dom = kernels[dom_key]
     stage_name = dom_key.split(".")[-1]
     traffic = traffic_from_profile(KERNEL_NAMES[stage_name], args.workload)
-    total_bytes = sum(u[s]["bytes"] for u in units for s in STAGES)
-    total_flops = sum(u[s]["flops"] for u in units for s in STAGES)
-    apply_ms = sum(sum(sm.values()) for sm in res["stage_ms"])
     T = wl.T
     tokens_per_s = T * ws / (step_ms * 1e-3)
     e2e = None
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = time_e2e(wl, ctx, max(8, args.steps // 2), 2, dev)
+        e2e_ms, h2d, d2h = time_e2e(wl, ctx, max(8, args.steps // 2), 3, dev)
         e2e_ms = max_over_ranks(e2e_ms)
         e2e = {"value": round(T * ws / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
                "overlap": "double-buffered: a step's host-to-device copies, kernels and device-to-host copy "
                           "overlap the neighbouring steps' on three streams"}
-    cpu = None
+    del ctx
+    torch.cuda.empty_cache()
+    cpu, per_workload = None, None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        rate, cores, sample, secs = cpu_oracle_rate(wl, args.cpu_seconds)
-        cpu = {"value": round(rate, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
-               "seconds": round(secs, 2)}
-    active = int(((np.repeat(wl.adapter_ids, wl.q_seq_lens)) != 0).sum())
+        c_all = cpu_oracle_rates(wl, 0, args.cpu_seconds)
+        cpu = {"value": c_all["tokens_per_s"], "unit": "tokens/s", "cores": c_all["threads"], "kind": "oracle",
+               "sample": c_all["sample"], "seconds": c_all["step_s"]}
+    if rank == 0 and not args.headline_only:
+        per_workload = per_workload_summary(args, dev, hbm_peak, bf16_peak, (wl.name, res, cpu is not None))
+    sb, sf = step_bytes(wl)
     line = {
         "metric": METRIC,
         "value": round(tokens_per_s, 1),
@@ -510,35 +602,29 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16 in, fp32 accumulate / fp32 y",
         "data": "synthetic (seeded PCG64; random-init adapters)",
-        "config": {"workload": wl.name, "tokens": T, "active_tokens": active, "sequences": wl.S,
-                   "slots": wl.num_slots,
-                   "projections": [{"name": p.name, "d_in": p.d_in, "lanes": p.lane_d_out, "max_rank": p.max_rank}
-                                   for p in wl.projections],
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
-                   "timing": "CUDA-graph replay of build_segments + apply per step (checked bit-exact against "
-                             "an eager step); per-kernel times from an eager pass with events between kernels",
-                   "parallelism": f"replicas x{ws} (no exchange)"},
+        "config": workload_config(wl, ws),
         "roofline": {"kernel": KERNEL_NAMES[stage_name] + (f" ({dom_key})" if "." in dom_key else ""),
                      "bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(dom["gbs"] / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
-        "step_roofline": {"alg_bytes": int(total_bytes), "flops": int(total_flops),
-                          "apply_ms": round(apply_ms, 5), "seg_build_ms": round(res["seg_ms"], 5),
-                          "gbs": round(total_bytes / (apply_ms * 1e-3) / 1e9, 1),
-                          "frac_hbm": round(total_bytes / (apply_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                          "tflops": round(total_flops / (apply_ms * 1e-3) / 1e12, 2),
-                          "frac_bf16": round(total_flops / (apply_ms * 1e-3) / 1e12 / bf16_peak, 5)},
+        "step_roofline": {"alg_bytes": int(sb), "flops": int(sf), "step_ms": round(step_ms, 5),
+                          "gbs": round(sb / (step_ms * 1e-3) / 1e9, 1),
+                          "frac_hbm": round(sb / (step_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "apply_ms": rec["apply_ms"], "frac_hbm_apply": rec["frac_hbm_apply"],
+                          "seg_build_ms": rec["seg_build_ms"],
+                          "tflops": round(sf / (step_ms * 1e-3) / 1e12, 2),
+                          "frac_bf16": round(sf / (step_ms * 1e-3) / 1e12 / bf16_peak, 5)},
         "kernels": kernels,
         "gpu_launches": int(res["launches"]),
-        "ms_per_step_eager": round(res["step_ms_eager"], 5),
-        "ms_per_step_median": round(res["step_ms_median"], 5),
+        "ms_per_step_eager": rec["ms_per_step_eager"],
+        "ms_per_step_median": rec["ms_per_step_median"],
         "clocks": res["clocks"],
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
-    if args.all_workloads and rank == 0:
-        line["per_workload"] = per_workload_summary(args, dev, hbm_peak)
+    if per_workload is not None:
+        line["per_workload"] = per_workload
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -546,26 +632,26 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def per_workload_summary(args, dev, hbm_peak):
+def per_workload_summary(args, dev, hbm_peak, bf16_peak, headline):
+    """Every configuration: device times and rooflines, and the oracle's
+    single-thread and all-core rates (the headline's timings are reused)."""
+    import torch
     out = {}
+    h_name, h_res, with_cpu = headline
     for name in W.CONFIG_NAMES:
-        if name == args.workload:
-            continue
         wl = W.make_workload(name, seed=args.seed)
-        res, _ = time_ours(wl, args.steps, args.warmup, dev, 0)
-        units = algorithmic_units(wl)
-        apply_ms = sum(sum(sm.values()) for sm in res["stage_ms"])
-        b = sum(u[s]["bytes"] for u in units for s in STAGES)
-        f = sum(u[s]["flops"] for u in units for s in STAGES)
-        out[name] = {"tokens": wl.T, "ms_per_step": round(res["step_ms"], 5),
-                     "ms_per_step_eager": round(res["step_ms_eager"], 5),
-                     "ms_per_step_median": round(res["step_ms_median"], 5),
-                     "tokens_per_s": round(wl.T / (res["step_ms"] * 1e-3), 1),
-                     "apply_ms": round(apply_ms, 5), "seg_build_ms": round(res["seg_ms"], 5),
-                     "alg_bytes": int(b), "gbs": round(b / (apply_ms * 1e-3) / 1e9, 1),
-                     "frac_hbm": round(b / (apply_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                     "tflops": round(f / (apply_ms * 1e-3) / 1e12, 2),
-                     "stage_ms": [{k: round(v, 5) for k, v in sm.items()} for sm in res["stage_ms"]]}
+        if name == h_name and not args.max_seqs:
+            res = h_res
+        else:
+            res, ctx = time_ours(wl, args.steps, args.warmup, dev, 0)
+            del ctx
+            torch.cuda.empty_cache()
+        rec = workload_record(wl, res, hbm_peak, bf16_peak)
+        rec["clocks"] = res["clocks"]
+        if with_cpu:
+            rec["cpu_oracle"] = {"threads_1": cpu_oracle_rates(wl, 1, args.cpu_seconds_detail),
+                                 "threads_all": cpu_oracle_rates(wl, 0, args.cpu_seconds_detail)}
+        out[name] = rec
     return out
 
 
@@ -579,12 +665,12 @@ def run_reference(args):
     wl = W.make_workload(args.workload, seed=args.seed, draw_xy=True)
     per_step_s = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_oracle_rate(wl, per_step_s * 0.5)
-    rates, secs = [], []
-    for s in range(args.steps):
-        rate, cores, sample, dt = cpu_oracle_rate(wl, per_step_s, seed=s)
-        rates.append(rate)
-        secs.append(dt)
+        cpu_oracle_rates(wl, 0, per_step_s * 0.5, runs=1)
+    rates, secs, last = [], [], None
+    for st in range(args.steps):
+        last = cpu_oracle_rates(wl, 0, per_step_s, runs=1, seed=st)
+        rates.append(last["tokens_per_s"])
+        secs.append(last["step_s"])
     value = statistics.mean(rates)
     line = {
         "impl": "reference",
@@ -600,9 +686,9 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded PCG64; random-init adapters)",
-        "config": {"workload": wl.name, "tokens": wl.T, "sequences": wl.S, "slots": wl.num_slots},
-        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: {sample}"},
+        "config": workload_config(wl, ws),
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": last["threads"], "kind": "oracle",
+                         "sample": f"each step: {last['sample']}"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -611,15 +697,18 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="cont_batch", choices=W.CONFIG_NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=3.0,
+                    help="oracle delta-phase time per run for the headline cpu_baseline (and the reference arm)")
+    ap.add_argument("--cpu-seconds-detail", type=float, default=0.5,
+                    help="oracle delta-phase time per run for each configuration's 1-thread / all-core rates")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--all-workloads", action="store_true", help="add a per_workload summary of the other configs")
+    ap.add_argument("--headline-only", action="store_true", help="skip the per_workload records of all configs")
     ap.add_argument("--max-seqs", type=int, default=0,
                     help="keep only the first N sequences of the workload (smaller case for profiler captures)")
     args = ap.parse_args()

@@ -81,14 +81,15 @@ typedef struct lora_segments lora_segments;
  * lane, bf16 factors of a rank r <= max_rank padded with zeros to
  * R16 = max_rank rounded up to a multiple of 16, a rank and an fp32 scale
  * (the caller computes scale = lora_alpha / r * strength).  The pool also
- * holds the rank-space scratch of up to max_tokens rows used between the
- * shrink and the expand kernels (fp32 partial sums, bf16 U tiles, and per-tile
- * counters that the zero fill starts at zero and every apply leaves at zero),
- * so two applies on one pool must be ordered on one stream.
+ * holds the tensor path's rank-space scratch for up to max_tokens rows, used
+ * between its shrink and expand kernels (fp32 partial sums, bf16 U tiles, and
+ * per-tile counters that the zero fill starts at zero and every apply leaves
+ * at zero), so two applies on one pool must be ordered on one stream.
  *
- * Shapes: d_in and every lane_d_out[l] must be positive multiples of 64;
+ * Shapes: d_in (<= 65536) and every lane_d_out[l] must be positive multiples of 64;
  * 1 <= num_lanes <= LORA_MAX_LANES; 2 <= num_slots <= LORA_MAX_SLOTS;
- * 1 <= max_rank <= 128 and num_lanes * R16 <= 256; max_tokens >= 1.
+ * 1 <= max_rank <= 128; max_tokens >= 1.  (The tensor path keeps a tile's
+ * num_lanes * R16 <= 512 rank columns of fp32 accumulators in tensor memory.)
  */
 
 /* Bytes of device memory a pool of this shape needs (0 if the shape is invalid). */
@@ -189,12 +190,14 @@ int lora_segments_destroy(lora_segments* seg);
  *      [off_l, off_l + lane_d_out[l]), off_l = sum of the earlier lanes' widths.
  * Rows of slot 0, and lanes of rank 0, are neither read nor written.  Each
  * row's result depends only on its own x row, its adapter's factors and its
- * own sequence's length: sums run in fp32 in a fixed order (decode path:
- * shrink over d_in in fixed 1024-wide chunks reduced by a fixed tree, expand
- * over the rank in ascending order, y = fma(scale, v, y); tensor path: tcgen05
- * bf16 MMAs with fp32 accumulation, the rank-space vector split into two bf16
- * halves for the expand, y = y + scale * v).
- * The decode-path kernels run on a side stream the library creates per device
+ * own sequence's length: sums run in fp32 in a fixed order that depends on
+ * d_in and the lane's rank only (decode path: one fused kernel per call, a
+ * thread-block cluster per (row group, lane) shrinks fixed K ranges of d_in,
+ * adds the ranges' partial sums in order on chip, expands over the rank in
+ * ascending order, y = fma(scale, v, y); tensor path: tcgen05 bf16 MMAs with
+ * fp32 accumulation, the rank-space vector split into two bf16 halves for the
+ * expand, y = y + scale * v).
+ * The decode-path kernel runs on a side stream the library creates per device
  * (forked from and joined back to `stream` with events), concurrently with the
  * tensor-path kernels on `stream`; the call stays ordered on `stream` and can
  * be stream-captured.
@@ -205,9 +208,9 @@ int lora_apply_shrink_expand(const lora_pool* pool, const lora_segments* seg, co
                              float* y, int64_t ldx, int64_t ldy, lora_stream_t stream);
 
 /* One kernel of lora_apply_shrink_expand, for per-kernel timing:
- * stage 1 = decode shrink, 2 = decode expand, 3 = tensor shrink, 4 = tensor
- * expand.  Running stages 1..4 in order on one stream gives exactly the
- * result of lora_apply_shrink_expand. */
+ * stage 1 = decode path (fused shrink -> expand), 2 = tensor shrink,
+ * 3 = tensor expand.  Running stages 1..3 in order on one stream gives
+ * exactly the result of lora_apply_shrink_expand. */
 int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void* x, float* y,
                      int64_t ldx, int64_t ldy, int stage, lora_stream_t stream);
 
@@ -216,13 +219,13 @@ int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void
  * only its input and output buffers, or a serving loop whose memory plan is
  * frozen after start-up.  No passage of the pages has a counterpart; this is a
  * property of the library, not of the method.
- *   - The rank-space intermediate lives in a fixed array compiled into the
- *     library, of LORA_NOALLOC_SCRATCH_BYTES; every GPU that loads the
- *     library holds it until the process exits.  A step needs, in floats,
- *     16448 (counters) + C * T * num_lanes * R16 (decode partial
- *     sums, C = ceil(d_in / 1024)) + 3 * (T / 64 + 1) * num_lanes * R16 * 128
- *     (tensor-path partial sums and U tiles); one that needs more returns
- *     LORA_ERR_SHAPE before anything is enqueued.
+ *   - The tensor path's rank-space intermediate lives in a fixed array
+ *     compiled into the library, of LORA_NOALLOC_SCRATCH_BYTES; every GPU
+ *     that loads the library holds it until the process exits.  A step needs,
+ *     in floats, 16384 (per-tile counters) + 3 * (T / 64 + 1) * num_lanes *
+ *     R16 * 128 (the tensor tiles' partial sums and U tiles); one that needs
+ *     more returns LORA_ERR_SHAPE before anything is enqueued.  (The decode
+ *     path keeps its rank-space vector on chip and needs no scratch.)
  *   - The call allocates nothing.  Its first call on a device looks up the
  *     array's device address (cudaGetSymbolAddress) with that device current;
  *     make that first call before any stream capture.  The current device must

@@ -55,7 +55,7 @@ def test_pool_bytes_shapes(lib):
     assert LD.lora_pool_bytes(9, 16, 4000, [4096], 1) == 0          # d_in not a multiple of 64
     assert LD.lora_pool_bytes(9, 16, 4096, [100], 1) == 0           # d_out not a multiple of 64
     assert LD.lora_pool_bytes(9, 129, 4096, [4096], 1) == 0         # rank above 128
-    assert LD.lora_pool_bytes(9, 128, 4096, [64, 64, 64], 1) == 0   # lanes x R16 > 256
+    assert LD.lora_pool_bytes(9, 128, 4096, [64] * 4, 1) > 0        # 4 lanes x R16 128 = 512 TMEM columns
     assert LD.lora_pool_bytes(9, 16, 4096, [64] * 5, 1) == 0        # more than 4 lanes
 
 

@@ -11,35 +11,43 @@
 // on one thread-block cluster of CL CTAs (CL from the pool's shape only):
 //   1. CTA c of the cluster shrinks its fixed range of d_in (K blocks of 64,
 //      [c * nkb / CL, (c + 1) * nkb / CL)) for the group's rows: a partial
-//      rank-space vector of 8 rows x r16 ranks, in its shared memory.
-//   2. Every CTA tells every CTA of the cluster that its partial is ready
-//      (remote mbarrier arrivals), then sums the CL partials in CTA order
-//      straight out of the other CTAs' shared memory (distributed shared
-//      memory).  So u never leaves the chip, and every CTA holds the same u.
+//      rank-space vector of up to 8 rows x r16 ranks.
+//   2. Every CTA pushes its partial into every CTA's shared memory with
+//      st.async, counted on the receiver's mbarrier (no fence, no global
+//      memory); each CTA then adds the CL partials in CTA order.  So u never
+//      leaves the chip, and every CTA of the cluster holds the same u.
 //   3. CTA c expands its own slice of the lane's output columns
 //      ([c * ncb / CL, (c + 1) * ncb / CL) in blocks of 64) and updates y.
-// A producer warp streams, in the order the compute warps use them, the
-// group's x rows of the K range (into an x buffer) and the slot's A rows
-// (TMA tiles, 128-byte swizzle) and then, per 512-column chunk, the group's y
-// rows and the slot's B^T rank rows (bulk copies) through a ring of 16 KB
-// pages, so the expand's first loads are in flight while the shrink and the
-// cluster exchange run.
+// The clusters are persistent (as many as fit on the GPU at once) and take
+// the units longest first (by rank class), dealt in snake order, so the
+// longest units start first and the clusters finish close together.
+// A producer warp streams, in the order the compute warps use them, pages of
+// the group's x rows with the slot's A rows for a few K blocks (bulk copies
+// and TMA tiles with the 128-byte swizzle) and then, per 512-column chunk,
+// the slot's B^T rank rows (TMA boxes of 16 ranks x up to 256 columns) and the
+// group's y rows (bulk copies), through a
+// ring of pages; the compute warps hold one page at a time, so the expand's
+// first loads are in flight while the shrink and the exchange run.
 //
 // Fixed summation order, independent of the group a row lands in (so a row's
 // bits depend only on its own x, its adapter and d_in):
-//  * shrink: in each A page a compute thread takes two 8-element K chunks
-//    (its K split s and s + nks); per (row, rank) it keeps an even-element and
-//    an odd-element fma chain over its chunks in K order, adds them, and the
-//    nks K splits of a rank tile are combined by a fixed xor butterfly inside
-//    one warp; the cluster's CL partials are then added in CTA order.
+//  * shrink: thread (rank tile of 4 ranks, K split ks) takes the 8-element K
+//    chunks ks, ks + nks, ks + 2 nks, ... of its CTA's K range (nks from r16
+//    only); per (row, rank) it keeps an even-element and an odd-element fma
+//    chain over its chunks in K order and adds them; the nks K splits are
+//    combined by a fixed xor butterfly inside one warp; the cluster's CL
+//    partials are then added in CTA order.
 //  * expand: v[o] accumulates B[o][i] * u[i] for i = 0..r-1 in order with fma;
 //    y = fma(scale, v, y).
 // The fmas are issued two at a time (packed f32x2), each exactly an fmaf in
-// the order above.  Every wait is bounded; a wait that gives up records
-// LORA_ERR_TIMEOUT and the CTA stops its work, still meeting its cluster
-// barriers, so no CTA leaves while another may read its shared memory.
+// the order above; the thread tiles cover 1, 2, 4 or 8 rows (the group's row
+// count rounded up), which changes no row's arithmetic.  Every wait is
+// bounded; a wait that gives up records LORA_ERR_TIMEOUT and the CTA stops
+// its work, still meeting its cluster barriers, so no CTA leaves while
+// another may still write into its shared memory.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -52,17 +60,18 @@ namespace {
 constexpr int kDfComputeWarps = 4;
 constexpr int kDfCompute = kDfComputeWarps * 32;  // compute threads
 constexpr int kDfThreads = kDfCompute + 32;       // + the producer warp
-constexpr int kDfPageBytes = 16384;               // ring page
-constexpr int kDfPages = 4;
+constexpr int kDfPageBytes = 18432;               // ring page (1024-aligned size)
+constexpr int kDfMaxPages = 12;                   // ring pages: as many as the shared memory left allows
+constexpr int kDfCtasPerSm = 2;                   // resident CTAs per SM the launch is sized for
 constexpr int kDfCols = 512;                      // expand columns per chunk, 4 per compute thread
 constexpr int kDfColsPerThread = kDfCols / kDfCompute;
-constexpr int kDfRanksPerPage = kDfPageBytes / (kDfCols * 2);  // B^T rank rows per page
-constexpr int kDfYPitch = kDfCols * 4;                         // bytes per y row of a page
-constexpr int kDfMaxCluster = 8;
-constexpr int kDfPartFloats = 128 * kDecGroup;  // a partial: [rank][row], ranks up to 128
+constexpr int kDfRanksPerPage = 16;               // B^T rank rows per page (16 x 512 bf16 = 16 KB)
+constexpr int kDfYPitch = kDfCols * 4;            // bytes per y row of a page
+constexpr int kDfUFloats = 128 * kDecGroup;       // u of a unit: [rank][row], ranks up to 128
 static_assert(kDfColsPerThread == 4, "expand thread tile: 4 columns x 8 rows");
-static_assert(kDecGroup * kDfYPitch == kDfPageBytes, "a y page holds the group's rows of one chunk");
-static_assert(kDfRanksPerPage == 16, "16 B^T rank rows per page");
+static_assert(kDecGroup * kDfYPitch <= kDfPageBytes, "a y page holds the group's rows of one chunk");
+static_assert(kDfRanksPerPage * kDfCols * 2 <= kDfPageBytes, "a B page holds 16 rank rows of one chunk");
+static_assert(kDfPageBytes % 1024 == 0, "pages keep the 1024-byte alignment of the A tiles");
 
 struct DfParams {
   const int32_t* counts;
@@ -71,13 +80,12 @@ struct DfParams {
   const int32_t* rank_tab;
   const float* scale_tab;
   int32_t* status;
-  const uint16_t* Bt[LORA_MAX_LANES];
   const uint16_t* x;
   int64_t ldx;
   float* y;
   int64_t ldy;
-  int L, R16, nkb, kc_max;
-  int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES];
+  int L, R16, nkb, npages;
+  int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES], bt_cols[LORA_MAX_LANES];
 };
 
 // Element l of a per-lane parameter array, read with constant indexes (a
@@ -99,7 +107,10 @@ struct Unit {
   int kb0, kb1;    // this CTA's K blocks of 64
   int c0, c1;      // this CTA's output columns of the lane
   int dout, off;
-  int nks, nkbp;   // K splits per rank tile; K blocks per A page
+  int bi;          // columns per B^T TMA box of the lane (the page holds ceil(ec / bi) boxes of 16 x bi)
+  int nks;         // K splits per rank tile
+  int nkbp;        // K blocks per A page
+  int cpt;         // 8-element K chunks per thread per A page (1 or 2)
 };
 
 __device__ __forceinline__ bool load_unit(const DfParams& p, int u, int cta, int ncta, Unit& U) {
@@ -118,6 +129,7 @@ __device__ __forceinline__ bool load_unit(const DfParams& p, int u, int cta, int
   U.kb1 = (cta + 1) * p.nkb / ncta;
   U.dout = lane_param(p.d_out, U.l);
   U.off = lane_param(p.off, U.l);
+  U.bi = lane_param(p.bt_cols, U.l);
   const int ncb = U.dout / 64;
   U.c0 = (cta * ncb / ncta) * 64;
   U.c1 = ((cta + 1) * ncb / ncta) * 64;
@@ -125,9 +137,83 @@ __device__ __forceinline__ bool load_unit(const DfParams& p, int u, int cta, int
   // compute threads are split evenly over them
   int nrt = 4;
   while (nrt * 4 < U.r16) nrt *= 2;
-  U.nks = kDfCompute / nrt;
-  U.nkbp = kDfPageBytes / (U.r16 * 128);  // = nks / 4: two 8-element chunks per thread per page
+  U.nks = kDfCompute / nrt;  // 32, 16, 8 or 4
+  // K blocks per A page: a power of two with the page within kDfPageBytes
+  // (x rows and A rows) and at most two chunks per thread
+  int nkbp = U.nks >= 8 ? U.nks / 4 : 1;
+  while (nkbp > 1 && nkbp * (kDecGroup + U.r16) * 128 > kDfPageBytes) nkbp >>= 1;
+  U.nkbp = nkbp;
+  U.cpt = 8 * nkbp / U.nks;
   return true;
+}
+
+// The units of one cluster, longest first.  Units are ranked by the rank
+// class of their (slot, lane), r16 / 16 (a unit's bytes and fmas grow with
+// its rank), highest class first and in unit order inside a class, and dealt
+// to the clusters in snake order (0, 1, .., nc-1, nc-1, .., 0, 0, ..), so the
+// longest units start first and every cluster gets a similar share.  Every
+// warp runs its own copy of the iterator (ballots over 32 units at a time),
+// so all warps of all CTAs of a cluster walk the same sequence; which cluster
+// runs a unit never changes its result.
+struct UnitIter {
+  int n_units, q, nc;
+  int cls;        // rank class being scanned (7..0), -1 when done
+  int u0;         // first unit of the next 32-unit chunk to scan
+  int base;       // units ranked before that chunk
+  int pbase;      // first unit of the chunk that pend refers to
+  unsigned pend;  // units of that chunk dealt to this cluster and not yet returned
+  unsigned present;
+};
+
+__device__ __forceinline__ int unit_class(const DfParams& p, int u) {
+  const int w = u / p.L, l = u - w * p.L;
+  const int r = p.rank_tab[p.work[w].x * p.L + l];
+  return r > 0 ? (r + 15) / 16 - 1 : -1;
+}
+
+__device__ __forceinline__ void unit_iter_init(UnitIter& it, const DfParams& p, int n_units, int lane) {
+  it.n_units = n_units;
+  it.q = (int)cluster_id_x();
+  it.nc = (int)num_clusters_x();
+  unsigned present = 0;
+  for (int u0 = 0; u0 < n_units; u0 += 32) {
+    const int c = u0 + lane < n_units ? unit_class(p, u0 + lane) : -1;
+    present |= __reduce_or_sync(0xffffffffu, c >= 0 ? 1u << c : 0u);
+  }
+  it.present = present;
+  it.cls = present ? 31 - __clz((int)present) : -1;
+  it.u0 = 0;
+  it.base = 0;
+  it.pbase = 0;
+  it.pend = 0;
+}
+
+// The next unit of this cluster (all 32 lanes call it together); false when done.
+__device__ __forceinline__ bool next_unit(UnitIter& it, const DfParams& p, int lane, int& u) {
+  for (;;) {
+    if (it.pend) {  // units of the last scanned chunk dealt to this cluster, in order
+      const int j = __ffs(it.pend) - 1;
+      it.pend &= it.pend - 1;
+      u = it.pbase + j;
+      return true;
+    }
+    if (it.cls < 0) return false;
+    if (it.u0 >= it.n_units) {  // this class is done: the next present one
+      const unsigned lower = it.present & ((1u << it.cls) - 1u);
+      it.cls = lower ? 31 - __clz((int)lower) : -1;
+      it.u0 = 0;
+      continue;
+    }
+    const int uu = it.u0 + lane;
+    const bool in = uu < it.n_units && unit_class(p, uu) == it.cls;
+    const unsigned m = __ballot_sync(0xffffffffu, in);
+    const int pos = (it.base + __popc(m & ((1u << lane) - 1u))) % (2 * it.nc);
+    const int owner = pos < it.nc ? pos : 2 * it.nc - 1 - pos;
+    it.pend = __ballot_sync(0xffffffffu, in && owner == it.q);
+    it.base += __popc(m);
+    it.pbase = it.u0;
+    it.u0 += 32;
+  }
 }
 
 // One step of a butterfly reduce-scatter: lanes exchange half of their values
@@ -143,138 +229,201 @@ __device__ __forceinline__ void rs_step(float* v, int lane, int o) {
   }
 }
 
+// The shrink's fmas over one A page for a tile of RT rows (RT = the group's
+// row count rounded up to 1, 2, 4 or 8): thread (rank tile rt, K split ks)
+// takes the page's 8-element K chunks ks (and ks + nks when cpt == 2).  A row's
+// chains do not depend on RT, so neither do its bits.  The page holds the x
+// rows [8][nkbp * 64] then the A rows [nkbp][r16][64] (128-byte swizzle).
+template <int RT>
+__device__ __forceinline__ void shrink_page(const uint8_t* pg, int nkbp, int r16, int rt, int ks, int nks, int cpt,
+                                            int nq, float2 (&acc)[kDecGroup][4]) {
+  const uint8_t* ap = pg + (size_t)kDecGroup * nkbp * 128;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int q = ks + h * nks;
+    if (h < cpt && q < nq) {
+      const int kbi = q >> 3, j = q & 7;
+      float2 a[4][4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int i = 4 * rt + jj;
+        const uint4 w = *reinterpret_cast<const uint4*>(ap + (size_t)(kbi * r16 + i) * 128 + ((j ^ (i & 7)) << 4));
+        a[jj][0] = make_float2(bf16lo(w.x), bf16hi(w.x));
+        a[jj][1] = make_float2(bf16lo(w.y), bf16hi(w.y));
+        a[jj][2] = make_float2(bf16lo(w.z), bf16hi(w.z));
+        a[jj][3] = make_float2(bf16lo(w.w), bf16hi(w.w));
+      }
+      const uint8_t* xq = pg + (size_t)q * 16;
+#pragma unroll
+      for (int g = 0; g < RT; ++g) {
+        const uint4 w = *reinterpret_cast<const uint4*>(xq + (size_t)g * nkbp * 128);
+        const float2 xp[4] = {make_float2(bf16lo(w.x), bf16hi(w.x)), make_float2(bf16lo(w.y), bf16hi(w.y)),
+                              make_float2(bf16lo(w.z), bf16hi(w.z)), make_float2(bf16lo(w.w), bf16hi(w.w))};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[g][jj] = ffma2(a[jj][e], xp[e], acc[g][jj]);
+      }
+    }
+  }
+}
+
+// The expand's fmas over one B^T page (nr rank rows starting at rank rb) for
+// a tile of RT rows: this thread's 4 columns (bp already offset to them in
+// its TMA box; pitch = the box's row bytes).
+template <int RT>
+__device__ __forceinline__ void expand_page(const uint8_t* bp, int pitch, const float* us, int rb, int nr,
+                                            float2 (&eacc)[kDecGroup][2]) {
+#pragma unroll 4
+  for (int ri = 0; ri < nr; ++ri) {
+    const uint2 q2 = *reinterpret_cast<const uint2*>(bp + (size_t)ri * pitch);
+    const float2 b01 = make_float2(bf16lo(q2.x), bf16hi(q2.x));
+    const float2 b23 = make_float2(bf16lo(q2.y), bf16hi(q2.y));
+    float ug[kDecGroup];
+    const float4 u0 = *reinterpret_cast<const float4*>(&us[(rb + ri) * kDecGroup]);
+    ug[0] = u0.x; ug[1] = u0.y; ug[2] = u0.z; ug[3] = u0.w;
+    if (RT > 4) {
+      const float4 u1 = *reinterpret_cast<const float4*>(&us[(rb + ri) * kDecGroup + 4]);
+      ug[4] = u1.x; ug[5] = u1.y; ug[6] = u1.z; ug[7] = u1.w;
+    }
+#pragma unroll
+    for (int g = 0; g < RT; ++g) {
+      const float2 u2 = make_float2(ug[g], ug[g]);
+      eacc[g][0] = ffma2(b01, u2, eacc[g][0]);
+      eacc[g][1] = ffma2(b23, u2, eacc[g][1]);
+    }
+  }
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-__global__ void __launch_bounds__(kDfThreads, 1)
-    dec_fused_kernel(const __grid_constant__ TmapSized tm_a, DfParams p) {
+__global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
+    dec_fused_kernel(const __grid_constant__ TmapSized tm_a, const __grid_constant__ TmapLanes tm_bt, DfParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kDfPages], empty_bar[kDfPages], xfull, xempty, pready[2];
-  __shared__ __align__(16) float part[2][kDfPartFloats];  // this CTA's partial u, [rank][row], per unit parity
-  __shared__ __align__(16) float us[kDfPartFloats];       // the summed u of the current unit, [rank][row]
+  __shared__ __align__(8) uint64_t full_bar[kDfMaxPages], empty_bar[kDfMaxPages], precv[2];
+  __shared__ __align__(16) float us[kDfUFloats];  // the summed u of the current unit, [rank][row]
   __shared__ int fail_sh;
   __shared__ int stop_sh[2];
+  __shared__ int xok_sh[2];  // per unit parity: every partial of the cluster arrived
 
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* ring = smem;                                              // kDfPages x 16 KB, 1024-aligned
-  uint16_t* xbuf = reinterpret_cast<uint16_t*>(smem + kDfPages * kDfPageBytes);  // [8][kc_max] bf16
+  const uint32_t npages = (uint32_t)p.npages;
+  uint8_t* ring = smem;  // npages pages, 1024-aligned
+  // partials received from the cluster's CTAs: [parity][ncta][R16 * 8] floats
+  float* recv = reinterpret_cast<float*>(smem + (size_t)npages * kDfPageBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = (int)cluster_ctarank(), ncta = (int)cluster_nctarank();
+  const int part_floats = p.R16 * kDecGroup;
   pdl_wait();  // the segment builder's results are visible from here on
   if (tid == 0) {
-    for (int s = 0; s < kDfPages; ++s) {
+    for (uint32_t s = 0; s < npages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kDfComputeWarps);
     }
-    mbar_init(&xfull, 1);
-    mbar_init(&xempty, kDfComputeWarps);
-    // one arrival from every CTA of the cluster per unit; two barriers used by
-    // unit parity, so a CTA already on the next unit can never arrive on the
-    // barrier of a unit that a slower CTA has not yet signalled
-    mbar_init(&pready[0], (uint32_t)ncta);
-    mbar_init(&pready[1], (uint32_t)ncta);
+    // per unit parity: one local arrival (with the expected bytes) and the
+    // st.async bytes of every CTA's partial
+    mbar_init(&precv[0], 1);
+    mbar_init(&precv[1], 1);
     fail_sh = 0;
     fence_mbar_init();
   }
-  // every CTA's barriers are initialised before any CTA arrives on them remotely
+  // every CTA's barriers are initialised before any CTA stores into it
   cluster_sync_all();
 
-  // Units (decode group, lane) are dealt to the clusters round-robin; every
-  // CTA of a cluster walks the same list.  The counts are final before this
-  // grid runs (the builder wrote them; a builder error leaves them at 0).
+  // Units (decode group, lane), longest first (UnitIter).  The counts are
+  // final before this grid runs (the builder wrote them; a builder error
+  // leaves them at 0).
   const int n_units = p.counts[2] * p.L;
-  const int first = (int)cluster_id_x(), stride = (int)num_clusters_x();
+  UnitIter it;
+  unit_iter_init(it, p, n_units, lane);
 
   if (warp == kDfComputeWarps) {
-    // ---------------- producer: x rows and A tiles of the K range, then per
-    // chunk the y rows and the B^T rank rows, in the order they are used
-    if (lane == 0) {
-      uint32_t fill = 0, xj = 0;
-      bool ok = true;
-      auto next_page = [&](uint32_t bytes) -> uint8_t* {
-        const int s = (int)(fill % kDfPages);
-        if (fill >= kDfPages && !mbar_wait_or_fail(&empty_bar[s], ((fill / kDfPages) - 1) & 1, &fail_sh)) {
-          fail_sh = 1;
-          ok = false;
-          return nullptr;
-        }
-        mbar_expect_tx(&full_bar[s], bytes);
-        return ring + (size_t)s * kDfPageBytes;
-      };
-      for (int u = first; u < n_units && ok; u += stride) {
-        Unit U;
-        if (!load_unit(p, u, cta, ncta, U)) continue;
-        const int kc = (U.kb1 - U.kb0) * 64;
-        if (kc > 0) {
-          if (xj >= 1 && !mbar_wait_or_fail(&xempty, (xj - 1) & 1, &fail_sh)) {
-            fail_sh = 1;
-            break;
-          }
-          mbar_expect_tx(&xfull, (uint32_t)(U.nrows * kc * 2));
+    // ---------------- producer: per A page the group's x rows and the slot's
+    // A tiles, then per chunk the B^T rank rows and the y rows, in the order
+    // they are used.  All 32 lanes walk the units (the iterator's ballots);
+    // lane 0 issues the copies.
+    uint32_t fill = 0;
+    bool ok = true;
+    auto next_page = [&](uint32_t bytes) -> uint8_t* {
+      const int s = (int)(fill % npages);
+      if (fill >= npages && !mbar_wait_or_fail(&empty_bar[s], ((fill / npages) - 1) & 1, &fail_sh)) {
+        fail_sh = 1;
+        ok = false;
+        return nullptr;
+      }
+      mbar_expect_tx(&full_bar[s], bytes);
+      return ring + (size_t)s * kDfPageBytes;
+    };
+    int u;
+    while (next_unit(it, p, lane, u)) {
+      Unit U;
+      if (lane == 0 && ok && load_unit(p, u, cta, ncta, U)) {
+        for (int kb = U.kb0; kb < U.kb1 && ok; kb += U.nkbp) {
+          const int n = min(U.nkbp, U.kb1 - kb);
+          uint8_t* pg = next_page((uint32_t)(n * (U.nrows + U.r16) * 128));
+          if (!pg) break;
+          ++fill;
+          uint64_t* fb = &full_bar[(fill - 1) % npages];
 #pragma unroll
           for (int g = 0; g < kDecGroup; ++g)
             if (g < U.nrows)
-              bulk_load(xbuf + (size_t)g * p.kc_max, p.x + (size_t)U.row[g] * p.ldx + (size_t)U.kb0 * 64,
-                        (uint32_t)(kc * 2), &xfull);
-          ++xj;
-          // A pages: nkbp K blocks of the slot's r16 rank rows each, one TMA
-          // tile per power-of-two part of r16 (rows past the rank are the
-          // pool's zero padding)
-          for (int kb = U.kb0; kb < U.kb1 && ok; kb += U.nkbp) {
-            const int n = min(U.nkbp, U.kb1 - kb);
-            uint8_t* pg = next_page((uint32_t)(n * U.r16 * 128));
-            if (!pg) break;
-            ++fill;
-            for (int i = 0; i < n; ++i) {
-              int row = 0;
-              for (int sz = kTmapSizes - 1; sz >= 0; --sz) {
-                const int rows = 16 << sz;
-                while (U.r16 - row >= rows) {
-                  tma_load_3d(pg + (size_t)(i * U.r16 + row) * 128, &tm_a.m[sz][U.l], (kb + i) * 64, row, U.k,
-                              &full_bar[(fill - 1) % kDfPages]);
-                  row += rows;
-                }
+              bulk_load(pg + (size_t)g * U.nkbp * 128, p.x + (size_t)U.row[g] * p.ldx + (size_t)kb * 64,
+                        (uint32_t)(n * 128), fb);
+          // A tiles: one per power-of-two part of r16 (rows past the rank are
+          // the pool's zero padding)
+          uint8_t* ap = pg + (size_t)kDecGroup * U.nkbp * 128;
+          for (int i = 0; i < n; ++i) {
+            int row = 0;
+            for (int sz = kTmapSizes - 1; sz >= 0; --sz) {
+              const int rows = 16 << sz;
+              while (U.r16 - row >= rows) {
+                tma_load_3d(ap + (size_t)(i * U.r16 + row) * 128, &tm_a.m[sz][U.l], (kb + i) * 64, row, U.k, fb);
+                row += rows;
               }
             }
           }
         }
-        const uint16_t* Bb = lane_param(p.Bt, U.l) + (size_t)U.k * p.R16 * U.dout;
         for (int c0 = U.c0; c0 < U.c1 && ok; c0 += kDfCols) {
           const int ec = min(kDfCols, U.c1 - c0);
-          uint8_t* yp = next_page((uint32_t)(U.nrows * ec * 4));
+          const int nbox = (ec + U.bi - 1) / U.bi;
+          for (int rb = 0; rb < U.r && ok; rb += kDfRanksPerPage) {
+            // 16 rank rows x bi columns per TMA box (rows past the rank are
+            // the pool's zero padding, columns past d_out read as zeros)
+            uint8_t* bp = next_page((uint32_t)(nbox * kDfRanksPerPage * U.bi * 2));
+            if (!bp) break;
+            ++fill;
+            for (int b = 0; b < nbox; ++b)
+              tma_load_3d(bp + (size_t)b * kDfRanksPerPage * U.bi * 2, &tm_bt.m[U.l], c0 + b * U.bi, rb, U.k,
+                          &full_bar[(fill - 1) % npages]);
+          }
+          uint8_t* yp = ok ? next_page((uint32_t)(U.nrows * ec * 4)) : nullptr;
           if (!yp) break;
           ++fill;
 #pragma unroll
           for (int g = 0; g < kDecGroup; ++g)
             if (g < U.nrows)
               bulk_load(yp + (size_t)g * kDfYPitch, p.y + (size_t)U.row[g] * p.ldy + U.off + c0, (uint32_t)(ec * 4),
-                        &full_bar[(fill - 1) % kDfPages]);
-          for (int rb = 0; rb < U.r && ok; rb += kDfRanksPerPage) {
-            const int nr = min(kDfRanksPerPage, U.r - rb);
-            uint8_t* bp = next_page((uint32_t)(nr * ec * 2));
-            if (!bp) break;
-            ++fill;
-            for (int i = 0; i < nr; ++i)
-              bulk_load(bp + (size_t)i * (kDfCols * 2), Bb + (size_t)(rb + i) * U.dout + c0, (uint32_t)(ec * 2),
-                        &full_bar[(fill - 1) % kDfPages]);
-          }
+                        &full_bar[(fill - 1) % npages]);
         }
       }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    }
+    if (lane == 0) {
       // Copies already issued land before the CTA may leave (after a failure
       // the compute warps may not have waited for them): the latest fill of
-      // every page and the latest x load, each a bounded wait.
-      for (uint32_t f = fill > kDfPages ? fill - kDfPages : 0; f < fill; ++f)
-        if (!mbar_wait_bounded(&full_bar[f % kDfPages], (f / kDfPages) & 1)) fail_sh = 1;
-      if (xj >= 1 && !mbar_wait_bounded(&xfull, (xj - 1) & 1)) fail_sh = 1;
+      // every page, each a bounded wait.
+      for (uint32_t f = fill > npages ? fill - npages : 0; f < fill; ++f)
+        if (!mbar_wait_bounded(&full_bar[f % npages], (f / npages) & 1)) fail_sh = 1;
     }
   } else {
     // ---------------- compute warps
     const int t = tid;
-    uint32_t use = 0, xj = 0, uj = 0, dj = 0;
-    const uint32_t part_addr0 = smem_u32(&part[0][0]);
-    for (int u = first; u < n_units; u += stride) {
+    uint32_t use = 0, uj = 0, dj = 0;
+    int u;
+    while (next_unit(it, p, lane, u)) {
       Unit U;
       if (!load_unit(p, u, cta, ncta, U)) continue;
       // one stop decision per unit for all compute threads
@@ -284,8 +433,12 @@ __global__ void __launch_bounds__(kDfThreads, 1)
       if (stop_sh[dj & 1]) break;
       ++dj;
       bool ok = true;
-      const int kc = (U.kb1 - U.kb0) * 64;
-      // ---- shrink of this CTA's K range: thread tile 8 rows x 4 ranks
+      float* rbuf = recv + (size_t)(uj & 1) * ncta * part_floats;
+      uint64_t* pr = &precv[uj & 1];
+      // this CTA expects every CTA's partial of this unit (st.async bytes)
+      if (t == 0) mbar_expect_tx(pr, (uint32_t)(ncta * U.r16 * kDecGroup * 4));
+      // ---- shrink of this CTA's K range: thread tile rtile rows x 4 ranks
+      const int rtile = U.nrows <= 1 ? 1 : U.nrows <= 2 ? 2 : U.nrows <= 4 ? 4 : 8;
       const int rt = t / U.nks, ks = t - rt * U.nks;
       const bool active = rt * 4 < U.r16;
       float2 acc[kDecGroup][4];  // (even-K, odd-K) sums of A[4 rt + j] . x[row]
@@ -293,58 +446,25 @@ __global__ void __launch_bounds__(kDfThreads, 1)
       for (int g = 0; g < kDecGroup; ++g)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[g][j] = make_float2(0.f, 0.f);
-      if (kc > 0) {
-        if (!mbar_wait_or_fail(&xfull, xj & 1, &fail_sh)) {
+      for (int kb = U.kb0; kb < U.kb1; kb += U.nkbp, ++use) {
+        const int s = (int)(use % npages);
+        if (ok && !mbar_wait_or_fail(&full_bar[s], (use / npages) & 1, &fail_sh)) {
           ok = false;
           fail_sh = 1;
         }
-        for (int kb = U.kb0; kb < U.kb1; kb += U.nkbp, ++use) {
-          const int s = (int)(use % kDfPages);
-          if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kDfPages) & 1, &fail_sh)) {
-            ok = false;
-            fail_sh = 1;
-          }
-          const int nq = min(U.nkbp, U.kb1 - kb) * 8;  // 8-element K chunks in this page
-          if (ok && active) {
-            const uint8_t* pg = ring + (size_t)s * kDfPageBytes;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int q = ks + h * U.nks;
-              if (q < nq) {
-                const int kbi = q >> 3, j = q & 7;
-                float2 a[4][4];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                  const int i = 4 * rt + jj;
-                  const uint4 w = *reinterpret_cast<const uint4*>(pg + (size_t)(kbi * U.r16 + i) * 128 +
-                                                                  ((j ^ (i & 7)) << 4));
-                  a[jj][0] = make_float2(bf16lo(w.x), bf16hi(w.x));
-                  a[jj][1] = make_float2(bf16lo(w.y), bf16hi(w.y));
-                  a[jj][2] = make_float2(bf16lo(w.z), bf16hi(w.z));
-                  a[jj][3] = make_float2(bf16lo(w.w), bf16hi(w.w));
-                }
-                const uint16_t* xq = xbuf + (size_t)(kb - U.kb0) * 64 + q * 8;
-#pragma unroll
-                for (int g = 0; g < kDecGroup; ++g) {
-                  const uint4 w = *reinterpret_cast<const uint4*>(xq + (size_t)g * p.kc_max);
-                  const float2 xp[4] = {make_float2(bf16lo(w.x), bf16hi(w.x)), make_float2(bf16lo(w.y), bf16hi(w.y)),
-                                        make_float2(bf16lo(w.z), bf16hi(w.z)), make_float2(bf16lo(w.w), bf16hi(w.w))};
-#pragma unroll
-                  for (int e = 0; e < 4; ++e)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) acc[g][jj] = ffma2(a[jj][e], xp[e], acc[g][jj]);
-                }
-              }
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty_bar[s]);
+        const int nq = min(U.nkbp, U.kb1 - kb) * 8;  // 8-element K chunks in this page
+        if (ok && active) {
+          const uint8_t* pg = ring + (size_t)s * kDfPageBytes;
+          if (rtile == 1) shrink_page<1>(pg, U.nkbp, U.r16, rt, ks, U.nks, U.cpt, nq, acc);
+          else if (rtile == 2) shrink_page<2>(pg, U.nkbp, U.r16, rt, ks, U.nks, U.cpt, nq, acc);
+          else if (rtile == 4) shrink_page<4>(pg, U.nkbp, U.r16, rt, ks, U.nks, U.cpt, nq, acc);
+          else shrink_page<8>(pg, U.nkbp, U.r16, rt, ks, U.nks, U.cpt, nq, acc);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xempty);  // this warp is done with the x rows
-        ++xj;
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
-      // ---- the nks K splits of a rank tile: a fixed butterfly inside the warp
+      // ---- the nks K splits of a rank tile: a fixed butterfly inside the
+      // warp; then this CTA's partial goes to every CTA of the cluster
       {
         float v[32];  // index row * 4 + j
 #pragma unroll
@@ -379,114 +499,96 @@ __global__ void __launch_bounds__(kDfThreads, 1)
           out0 = 8 * (lane & 3);
           nout = 8;
         }
-        float* pt = part[uj & 1];
         if (active) {
+          // slot `cta` of every CTA's receive buffer, counted on its barrier
+          const uint32_t slot = smem_u32(rbuf + (size_t)cta * part_floats), bar = smem_u32(pr);
+          for (int c = 0; c < ncta; ++c) {
+            const uint32_t dst = mapa_shared(slot, (uint32_t)c), dbar = mapa_shared(bar, (uint32_t)c);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (e < nout) {
-              const int o = out0 + e, g = o >> 2, i = 4 * rt + (o & 3);
-              pt[i * kDecGroup + g] = v[e];
+            for (int e = 0; e < 8; ++e) {
+              if (e < nout) {
+                const int o = out0 + e, g = o >> 2, i = 4 * rt + (o & 3);
+                st_async_f32(dst + 4u * (uint32_t)(i * kDecGroup + g), v[e], dbar);
+              }
             }
           }
         }
       }
-      // ---- cluster exchange: every CTA's partial is ready, then u = the sum
-      // of the CL partials in CTA order
-      named_bar_sync(1, kDfCompute);  // this CTA's partial is complete
-      uint64_t* pr = &pready[uj & 1];
+      // ---- u = the sum of the CL partials in CTA order: one thread waits for
+      // the bytes, then releases the other compute threads
       if (t == 0) {
-        fence_acq_rel_cluster();
-        for (int c = 0; c < ncta; ++c) mbar_arrive_cluster(mapa_shared(smem_u32(pr), (uint32_t)c));
+        const bool got = mbar_wait_or_fail(pr, (uj >> 1) & 1, &fail_sh);
+        if (!got) fail_sh = 1;
+        xok_sh[uj & 1] = got ? 1 : 0;
       }
-      if (!mbar_wait_cluster_or_fail(pr, (uj >> 1) & 1, &fail_sh)) {
-        ok = false;
-        fail_sh = 1;
-      }
+      named_bar_sync(1, kDfCompute);
+      if (!xok_sh[uj & 1]) ok = false;
       if (ok) {
-        const uint32_t pa = part_addr0 + (uj & 1) * (uint32_t)(kDfPartFloats * 4);
         for (int idx = t; idx < U.r16 * kDecGroup; idx += kDfCompute) {
-          float vals[kDfMaxCluster];
-#pragma unroll
-          for (int c = 0; c < kDfMaxCluster; ++c)
-            if (c < ncta) vals[c] = ld_dsmem_f32(mapa_shared(pa + 4u * (uint32_t)idx, (uint32_t)c));
-          float sum = vals[0];
-#pragma unroll
-          for (int c = 1; c < kDfMaxCluster; ++c)
-            if (c < ncta) sum += vals[c];
+          float sum = rbuf[idx];
+          for (int c = 1; c < ncta; ++c) sum += rbuf[(size_t)c * part_floats + idx];
           us[idx] = sum;
         }
       }
       ++uj;
       named_bar_sync(1, kDfCompute);  // u complete
-      // ---- expand of this CTA's columns: thread tile 8 rows x 4 columns
+      // ---- expand of this CTA's columns: thread tile rtile rows x 4 columns
       const float sc = p.scale_tab[U.k * p.L + U.l];
+      // this thread's columns 4t..4t+3 of a chunk sit in TMA box 4t / bi of a B page
+      const int b_box = (kDfColsPerThread * t) / U.bi;
+      const int b_off = b_box * kDfRanksPerPage * U.bi * 2 + ((kDfColsPerThread * t) - b_box * U.bi) * 2;
       for (int c0 = U.c0; c0 < U.c1; c0 += kDfCols) {
         const int ec = min(kDfCols, U.c1 - c0);
         const bool has = kDfColsPerThread * t < ec;
-        // the y page: read this thread's values, then release the page
-        float4 yv[kDecGroup];
-        {
-          const int s = (int)(use % kDfPages);
-          if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kDfPages) & 1, &fail_sh)) {
-            ok = false;
-            fail_sh = 1;
-          }
-          const uint8_t* yp = ring + (size_t)s * kDfPageBytes + 16 * t;
-#pragma unroll
-          for (int g = 0; g < kDecGroup; ++g)
-            if (ok && has && g < U.nrows) yv[g] = *reinterpret_cast<const float4*>(yp + (size_t)g * kDfYPitch);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty_bar[s]);
-          ++use;
-        }
         float2 eacc[kDecGroup][2];  // columns (4t, 4t+1) and (4t+2, 4t+3) of each row
 #pragma unroll
         for (int g = 0; g < kDecGroup; ++g) eacc[g][0] = eacc[g][1] = make_float2(0.f, 0.f);
         for (int rb = 0; rb < U.r; rb += kDfRanksPerPage, ++use) {
-          const int s = (int)(use % kDfPages);
-          if (ok && !mbar_wait_or_fail(&full_bar[s], (use / kDfPages) & 1, &fail_sh)) {
+          const int s = (int)(use % npages);
+          if (ok && !mbar_wait_or_fail(&full_bar[s], (use / npages) & 1, &fail_sh)) {
             ok = false;
             fail_sh = 1;
           }
           if (ok && has) {
-            const uint8_t* bp = ring + (size_t)s * kDfPageBytes + 8 * t;
+            const uint8_t* bp = ring + (size_t)s * kDfPageBytes + b_off;
             const int nr = min(kDfRanksPerPage, U.r - rb);
-#pragma unroll 4
-            for (int ri = 0; ri < nr; ++ri) {
-              const uint2 q2 = *reinterpret_cast<const uint2*>(bp + (size_t)ri * (kDfCols * 2));
-              const float2 b01 = make_float2(bf16lo(q2.x), bf16hi(q2.x));
-              const float2 b23 = make_float2(bf16lo(q2.y), bf16hi(q2.y));
-              const float4 u0 = *reinterpret_cast<const float4*>(&us[(rb + ri) * kDecGroup]);
-              const float4 u1 = *reinterpret_cast<const float4*>(&us[(rb + ri) * kDecGroup + 4]);
-              const float ug[kDecGroup] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            if (rtile == 1) expand_page<1>(bp, 2 * U.bi, us, rb, nr, eacc);
+            else if (rtile == 2) expand_page<2>(bp, 2 * U.bi, us, rb, nr, eacc);
+            else if (rtile == 4) expand_page<4>(bp, 2 * U.bi, us, rb, nr, eacc);
+            else expand_page<8>(bp, 2 * U.bi, us, rb, nr, eacc);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[s]);
+        }
+        // the y page (streamed after the chunk's B pages): y = fma(scale, v, y)
+        {
+          const int s = (int)(use % npages);
+          if (ok && !mbar_wait_or_fail(&full_bar[s], (use / npages) & 1, &fail_sh)) {
+            ok = false;
+            fail_sh = 1;
+          }
+          if (ok && has) {
+            const uint8_t* yp = ring + (size_t)s * kDfPageBytes + 16 * t;
 #pragma unroll
-              for (int g = 0; g < kDecGroup; ++g) {
-                const float2 u2 = make_float2(ug[g], ug[g]);
-                eacc[g][0] = ffma2(b01, u2, eacc[g][0]);
-                eacc[g][1] = ffma2(b23, u2, eacc[g][1]);
+            for (int g = 0; g < kDecGroup; ++g) {
+              if (g < U.nrows) {
+                float4 a = *reinterpret_cast<const float4*>(yp + (size_t)g * kDfYPitch);
+                a.x = fmaf(sc, eacc[g][0].x, a.x);
+                a.y = fmaf(sc, eacc[g][0].y, a.y);
+                a.z = fmaf(sc, eacc[g][1].x, a.z);
+                a.w = fmaf(sc, eacc[g][1].y, a.w);
+                *reinterpret_cast<float4*>(p.y + (size_t)U.row[g] * p.ldy + U.off + c0 + kDfColsPerThread * t) = a;
               }
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty_bar[s]);
-        }
-        if (ok && has) {
-#pragma unroll
-          for (int g = 0; g < kDecGroup; ++g) {
-            if (g < U.nrows) {
-              float4 a = yv[g];
-              a.x = fmaf(sc, eacc[g][0].x, a.x);
-              a.y = fmaf(sc, eacc[g][0].y, a.y);
-              a.z = fmaf(sc, eacc[g][1].x, a.z);
-              a.w = fmaf(sc, eacc[g][1].y, a.w);
-              *reinterpret_cast<float4*>(p.y + (size_t)U.row[g] * p.ldy + U.off + c0 + kDfColsPerThread * t) = a;
-            }
-          }
+          ++use;
         }
       }
     }
   }
-  // no CTA leaves while another CTA of its cluster may still read its partials
+  // no CTA leaves while another CTA of its cluster may still store into it
   cluster_sync_all();
   if (tid == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
 }
@@ -497,17 +599,37 @@ int dec_group_bound(const PoolView& pool, const lora_segments* seg) {
   return ceil_div(T, kDecGroup) + (pool.N < T ? pool.N : T);
 }
 
-// CTAs per cluster: a function of the pool's shape only (d_in), so a row's
-// K split, and with it its bits, never depends on the batch.
+// CTAs per cluster: a function of d_in only, so a row's K split, and with it
+// its bits, depends neither on the batch nor on the pool's rank padding.
 int cluster_size(const PoolView& pool) {
   const int nkb = pool.d_in / 64;
-  return nkb >= kDfMaxCluster ? kDfMaxCluster : (nkb >= 4 ? 4 : (nkb >= 2 ? 2 : 1));
+  return nkb >= 4 ? 4 : (nkb >= 2 ? 2 : 1);
 }
 
-size_t dec_smem_bytes(const PoolView& pool, int ncta) {
-  const int nkb = pool.d_in / 64;
-  const int kc_max = ceil_div(nkb, ncta) * 64;
-  return 1024 + (size_t)kDfPages * kDfPageBytes + (size_t)kDecGroup * kc_max * 2;
+// Ring pages: as many 18 KB pages as the shared memory left to each of the
+// kDfCtasPerSm CTAs of an SM holds after the receive buffers (deep rings keep
+// more bytes in flight per CTA; a page round trip is a few microseconds).
+int dec_pages(const PoolView& pool, int ncta) {
+  static std::atomic<int> static_smem{-1};
+  int st = static_smem.load(std::memory_order_relaxed);
+  if (st < 0) {
+    cudaFuncAttributes fa;
+    st = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(dec_fused_kernel)) == cudaSuccess
+             ? (int)fa.sharedSizeBytes
+             : 8192;
+    static_smem.store(st, std::memory_order_relaxed);
+  }
+  // per-SM shared memory 228 KiB, 1 KiB of it reserved per resident CTA; at
+  // most 227 KiB per CTA
+  long long per_cta = 233472 / kDfCtasPerSm - 1024;
+  if (per_cta > 232448) per_cta = 232448;
+  const long long recv = 2LL * ncta * pool.R16 * kDecGroup * 4;
+  const long long pages = (per_cta - st - 1024 - recv) / kDfPageBytes;
+  return (int)(pages < kDfMaxPages ? pages : kDfMaxPages);
+}
+
+size_t dec_smem_bytes(const PoolView& pool, int ncta, int npages) {
+  return 1024 + (size_t)npages * kDfPageBytes + (size_t)2 * ncta * pool.R16 * kDecGroup * 4;
 }
 
 // Clusters that can be resident at once, per (device, cluster size, shared memory).
@@ -550,12 +672,13 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
   const long long units = (long long)dec_group_bound(pool, seg) * pool.L;
   if (units <= 0) return LORA_OK;
   const int ncta = cluster_size(pool);
-  const size_t smem = dec_smem_bytes(pool, ncta);
-  if (smem > 227 * 1024) return LORA_ERR_SHAPE;
+  const int npages = dec_pages(pool, ncta);
+  if (npages < 3) return LORA_ERR_SHAPE;
+  const size_t smem = dec_smem_bytes(pool, ncta, npages);
   if (!set_smem_limit(reinterpret_cast<const void*>(dec_fused_kernel), pool.device, (int)smem)) return LORA_ERR_CUDA;
-  // Two waves of resident clusters at most; a cluster takes units
-  // round-robin, so a step with more units reuses the clusters.
-  const long long cap = 2LL * max_active_clusters(pool.device, ncta, smem);
+  // Persistent clusters: as many as can be resident at once (each takes its
+  // share of the units), never more than there can be units.
+  const long long cap = max_active_clusters(pool.device, ncta, smem);
   const int clusters = (int)(units < cap ? units : cap);
   DfParams p{};
   p.counts = seg->counts;
@@ -565,9 +688,9 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
   p.scale_tab = pool.scale_tab;
   p.status = seg->status;
   for (int l = 0; l < LORA_MAX_LANES; ++l) {
-    p.Bt[l] = pool.Bt[l];
     p.d_out[l] = pool.d_out[l];
     p.off[l] = pool.off[l];
+    p.bt_cols[l] = bt_box_cols(pool.d_out[l] > 0 ? pool.d_out[l] : 64);
   }
   p.x = x;
   p.ldx = ldx;
@@ -576,7 +699,7 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
   p.L = pool.L;
   p.R16 = pool.R16;
   p.nkb = pool.d_in / 64;
-  p.kc_max = ceil_div(p.nkb, ncta) * 64;
+  p.npages = npages;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * ncta));
   cfg.blockDim = dim3(kDfThreads);
@@ -591,7 +714,7 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, dec_fused_kernel, pool.tm_a, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dec_fused_kernel, pool.tm_a, pool.tm_bt, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "dec_fused_kernel launch");
 }

@@ -183,6 +183,16 @@ __device__ __forceinline__ bool mbar_wait_cluster_or_fail(uint64_t* bar, uint32_
   }
 }
 
+// Store 4 bytes into the shared memory of any CTA of the cluster (a
+// shared::cluster address from mapa_shared) and count them on that CTA's
+// mbarrier (complete_tx): the receiver that sees the barrier's phase complete
+// sees the data, with no fence on the sending side.
+__device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "f"(v), "r"(cluster_bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Every thread of every CTA of the cluster arrives and waits (release /

@@ -35,6 +35,11 @@ constexpr int kTmapSizes = 4;
 // Tensor tiles a build can make: a sequence of q_len >= 64 gives at most
 // q_len / 64 tiles, so T rows give at most T / 64.
 inline int tc_tile_cap(int max_tokens) { return max_tokens / LORA_TC_MIN_QLEN + 1; }
+struct TmapLanes {
+  CUtensorMap m[LORA_MAX_LANES];
+};
+// Inner box width (columns) of the Bt maps of a lane of d_out columns.
+inline int bt_box_cols(int d_out) { return d_out < 256 ? d_out : 256; }
 struct TmapSized {
   CUtensorMap m[kTmapSizes][LORA_MAX_LANES];
 };
@@ -68,6 +73,7 @@ struct PoolView {
   int32_t* tile_cnt = nullptr;        // [tiles] K-range CTAs of a tile that finished (0 between calls)
   TmapSized tm_a;                     // A, 3-D {d_in, R16, N}, box {64, 16<<s, 1}, 128-byte swizzle
   TmapSized tm_bk;                    // Bk, 3-D {16, d_out, R16/16*N}, box {16, 128, 1<<s}, 32-byte swizzle
+  TmapLanes tm_bt;                    // Bt, 3-D {d_out, R16, N}, box {min(256, d_out), 16, 1}, no swizzle
 };
 
 }  // namespace lora

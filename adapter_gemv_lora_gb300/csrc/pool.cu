@@ -165,8 +165,20 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   pp->h_rank.assign((size_t)num_slots * num_lanes, 0);
   std::memset(&p->tm_a, 0, sizeof(p->tm_a));
   std::memset(&p->tm_bk, 0, sizeof(p->tm_bk));
+  std::memset(&p->tm_bt, 0, sizeof(p->tm_bt));
   for (int l = 0; l < num_lanes; ++l) {
     const uint64_t R16 = (uint64_t)P.R16;
+    {
+      // Bt as 16 rank rows x up to 256 columns per box (decode expand pages)
+      const uint64_t dims[3] = {(uint64_t)lane_d_out[l], R16, (uint64_t)num_slots};
+      const uint64_t strides[2] = {2ull * lane_d_out[l], 2ull * lane_d_out[l] * R16};
+      const uint32_t box[3] = {(uint32_t)bt_box_cols(lane_d_out[l]), 16u, 1u};
+      if (!encode_tmap(&p->tm_bt.m[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->Bt[l], dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        delete pp;
+        return LORA_ERR_CUDA;
+      }
+    }
     for (int sz = 0; sz < kTmapSizes; ++sz) {
       if ((16u << sz) <= R16) {
         const uint64_t dims[3] = {(uint64_t)d_in, R16, (uint64_t)num_slots};

@@ -68,6 +68,7 @@ constexpr int kDfColsPerThread = kDfCols / kDfCompute;
 constexpr int kDfRanksPerPage = 16;               // B^T rank rows per page (16 x 512 bf16 = 16 KB)
 constexpr int kDfYPitch = kDfCols * 4;            // bytes per y row of a page
 constexpr int kDfUFloats = 128 * kDecGroup;       // u of a unit: [rank][row], ranks up to 128
+constexpr int kDfClassCache = 2048;               // units whose rank class is kept in shared memory
 static_assert(kDfColsPerThread == 4, "expand thread tile: 4 columns x 8 rows");
 static_assert(kDecGroup * kDfYPitch <= kDfPageBytes, "a y page holds the group's rows of one chunk");
 static_assert(kDfRanksPerPage * kDfCols * 2 <= kDfPageBytes, "a B page holds 16 rank rows of one chunk");
@@ -85,6 +86,7 @@ struct DfParams {
   float* y;
   int64_t ldy;
   int L, R16, nkb, npages;
+  int parts;  // column parts per (group, lane), each its own unit (set on the device per step)
   int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES], bt_cols[LORA_MAX_LANES];
 };
 
@@ -114,8 +116,10 @@ struct Unit {
 };
 
 __device__ __forceinline__ bool load_unit(const DfParams& p, int u, int cta, int ncta, Unit& U) {
-  const int w = u / p.L;
-  U.l = u - w * p.L;
+  const int per_group = p.L * p.parts;
+  const int w = u / per_group, rem = u - w * per_group;
+  U.l = rem / p.parts;
+  const int part = rem - U.l * p.parts;
   const int4 g = p.work[w];
   const int4 r0 = p.dec_rows[2 * w], r1 = p.dec_rows[2 * w + 1];
   U.k = g.x;
@@ -130,9 +134,11 @@ __device__ __forceinline__ bool load_unit(const DfParams& p, int u, int cta, int
   U.dout = lane_param(p.d_out, U.l);
   U.off = lane_param(p.off, U.l);
   U.bi = lane_param(p.bt_cols, U.l);
+  // this unit's column part, then this CTA's share of it (blocks of 64)
   const int ncb = U.dout / 64;
-  U.c0 = (cta * ncb / ncta) * 64;
-  U.c1 = ((cta + 1) * ncb / ncta) * 64;
+  const int pb0 = part * ncb / p.parts, pb1 = (part + 1) * ncb / p.parts;
+  U.c0 = (pb0 + cta * (pb1 - pb0) / ncta) * 64;
+  U.c1 = (pb0 + (cta + 1) * (pb1 - pb0) / ncta) * 64;
   // rank tiles of 4 ranks, their count rounded up to a power of two; the
   // compute threads are split evenly over them
   int nrt = 4;
@@ -165,19 +171,27 @@ struct UnitIter {
   unsigned present;
 };
 
-__device__ __forceinline__ int unit_class(const DfParams& p, int u) {
-  const int w = u / p.L, l = u - w * p.L;
+__device__ __forceinline__ int unit_class_global(const DfParams& p, int u) {
+  const int per_group = p.L * p.parts;
+  const int w = u / per_group, l = (u - w * per_group) / p.parts;
   const int r = p.rank_tab[p.work[w].x * p.L + l];
   return r > 0 ? (r + 15) / 16 - 1 : -1;
 }
 
-__device__ __forceinline__ void unit_iter_init(UnitIter& it, const DfParams& p, int n_units, int lane) {
+// A unit's rank class: from the shared-memory copy filled at kernel start
+// (the first kDfClassCache units), else from global memory.
+__device__ __forceinline__ int unit_class(const DfParams& p, const int8_t* cls_sh, int u) {
+  return u < kDfClassCache ? (int)cls_sh[u] : unit_class_global(p, u);
+}
+
+__device__ __forceinline__ void unit_iter_init(UnitIter& it, const DfParams& p, const int8_t* cls_sh, int n_units,
+                                               int lane) {
   it.n_units = n_units;
   it.q = (int)cluster_id_x();
   it.nc = (int)num_clusters_x();
   unsigned present = 0;
   for (int u0 = 0; u0 < n_units; u0 += 32) {
-    const int c = u0 + lane < n_units ? unit_class(p, u0 + lane) : -1;
+    const int c = u0 + lane < n_units ? unit_class(p, cls_sh, u0 + lane) : -1;
     present |= __reduce_or_sync(0xffffffffu, c >= 0 ? 1u << c : 0u);
   }
   it.present = present;
@@ -189,7 +203,7 @@ __device__ __forceinline__ void unit_iter_init(UnitIter& it, const DfParams& p, 
 }
 
 // The next unit of this cluster (all 32 lanes call it together); false when done.
-__device__ __forceinline__ bool next_unit(UnitIter& it, const DfParams& p, int lane, int& u) {
+__device__ __forceinline__ bool next_unit(UnitIter& it, const DfParams& p, const int8_t* cls_sh, int lane, int& u) {
   for (;;) {
     if (it.pend) {  // units of the last scanned chunk dealt to this cluster, in order
       const int j = __ffs(it.pend) - 1;
@@ -205,7 +219,7 @@ __device__ __forceinline__ bool next_unit(UnitIter& it, const DfParams& p, int l
       continue;
     }
     const int uu = it.u0 + lane;
-    const bool in = uu < it.n_units && unit_class(p, uu) == it.cls;
+    const bool in = uu < it.n_units && unit_class(p, cls_sh, uu) == it.cls;
     const unsigned m = __ballot_sync(0xffffffffu, in);
     const int pos = (it.base + __popc(m & ((1u << lane) - 1u))) % (2 * it.nc);
     const int owner = pos < it.nc ? pos : 2 * it.nc - 1 - pos;
@@ -307,6 +321,7 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
   __shared__ int fail_sh;
   __shared__ int stop_sh[2];
   __shared__ int xok_sh[2];  // per unit parity: every partial of the cluster arrived
+  __shared__ int8_t cls_sh[kDfClassCache];  // rank class of each unit (-1: nothing to do)
 
   uint8_t* smem = align1024(smem_raw);
   const uint32_t npages = (uint32_t)p.npages;
@@ -336,9 +351,22 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
   // Units (decode group, lane), longest first (UnitIter).  The counts are
   // final before this grid runs (the builder wrote them; a builder error
   // leaves them at 0).
-  const int n_units = p.counts[2] * p.L;
+  // Column parts: when the step has fewer (group, lane) pairs than there are
+  // clusters, each pair's columns are split into up to 4 parts (a power of
+  // two), each its own unit that redoes the pair's shrink, so more clusters
+  // work.  Every CTA computes the same value from the same counts, and a
+  // row's bits do not depend on it.
+  {
+    const int pairs = p.counts[2] * p.L;
+    int parts = 1;
+    while (parts < 4 && pairs * parts * 2 <= (int)num_clusters_x()) parts *= 2;
+    p.parts = parts;
+  }
+  const int n_units = p.counts[2] * p.L * p.parts;
+  for (int u = tid; u < n_units && u < kDfClassCache; u += kDfThreads) cls_sh[u] = (int8_t)unit_class_global(p, u);
+  __syncthreads();
   UnitIter it;
-  unit_iter_init(it, p, n_units, lane);
+  unit_iter_init(it, p, cls_sh, n_units, lane);
 
   if (warp == kDfComputeWarps) {
     // ---------------- producer: per A page the group's x rows and the slot's
@@ -358,7 +386,7 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
       return ring + (size_t)s * kDfPageBytes;
     };
     int u;
-    while (next_unit(it, p, lane, u)) {
+    while (next_unit(it, p, cls_sh, lane, u)) {
       Unit U;
       if (lane == 0 && ok && load_unit(p, u, cta, ncta, U)) {
         for (int kb = U.kb0; kb < U.kb1 && ok; kb += U.nkbp) {
@@ -423,7 +451,7 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
     const int t = tid;
     uint32_t use = 0, uj = 0, dj = 0;
     int u;
-    while (next_unit(it, p, lane, u)) {
+    while (next_unit(it, p, cls_sh, lane, u)) {
       Unit U;
       if (!load_unit(p, u, cta, ncta, U)) continue;
       // one stop decision per unit for all compute threads
@@ -669,7 +697,8 @@ int max_active_clusters(int device, int ncta, size_t smem) {
 
 int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx, float* y,
                   int64_t ldy, cudaStream_t st) {
-  const long long units = (long long)dec_group_bound(pool, seg) * pool.L;
+  // units: (group, lane) pairs, each in up to 4 column parts
+  const long long units = (long long)dec_group_bound(pool, seg) * pool.L * 4;
   if (units <= 0) return LORA_OK;
   const int ncta = cluster_size(pool);
   const int npages = dec_pages(pool, ncta);
@@ -700,6 +729,7 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
   p.R16 = pool.R16;
   p.nkb = pool.d_in / 64;
   p.npages = npages;
+  p.parts = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * ncta));
   cfg.blockDim = dim3(kDfThreads);

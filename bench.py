@@ -454,7 +454,9 @@ def cpu_oracle_rates(wl, threads: int, target_s: float, runs: int = 3, seed: int
     tokens/s = T / (metadata time + T * delta time per row)."""
     import oracle
     oracle.build()
-    cores = oracle.max_threads() if threads <= 0 else threads
+    # all cores = the host's usable cores (a 1-thread run leaves OpenMP's
+    # default thread count at 1, so it is not asked)
+    cores = len(os.sched_getaffinity(0)) if threads <= 0 else threads
     rng = np.random.default_rng(seed)
     meta_t = []
     for _ in range(runs):

@@ -99,6 +99,8 @@ struct lora_segments {
   int4* dec_work = nullptr;
   int32_t* dec_rows = nullptr;  // [cap_dec][kDecGroup] the rows of each decode group (its perm entries)
   int4* tc_work = nullptr;
+  int32_t* run_ids = nullptr;   // [max_seqs] per-run slots of a dispatched-row (MoE) build
+  int32_t* run_lens = nullptr;  // [max_seqs] per-run lengths; the run count is counts[8]
 };
 
 namespace lora {
@@ -129,8 +131,12 @@ int run_stage(const PoolView& pool, const lora_segments* seg, const void* x, flo
 bool ensure_side_stream();
 
 // Launchers (return a LORA_* status).
+// S_dev: if set, the builder reads the sequence count there (at most S, the
+// capacity its shared memory is laid out for).
 int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens, int S, int T,
-                     cudaStream_t st);
+                     cudaStream_t st, const int32_t* S_dev = nullptr);
+int launch_moe_runs(lora_segments* seg, const int32_t* row_expert, const int32_t* row_adapter,
+                    const int32_t* row_seq, int T, int E, int A, cudaStream_t st);
 int launch_repack(const PoolView& pool, int slot, int lane, int rank, float scale, const uint16_t* A,
                   const uint16_t* B, cudaStream_t st);
 // Launch `kernel` allowing programmatic dependent launch on `st` (the kernel

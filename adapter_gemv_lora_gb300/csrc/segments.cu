@@ -33,6 +33,7 @@ struct SegParams {
   const int32_t* ids;
   const int32_t* lens;
   int S, T, N;
+  const int32_t* S_dev;  // if set, the sequence count is read here (at most S, the layout's capacity)
   int32_t* status;
   int32_t* counts;
   int32_t* seq_start;
@@ -167,15 +168,15 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   pdl_launch_next();  // the apply kernels may be scheduled now; they wait for this grid
   pdl_wait();         // the previous kernel's results are visible from here on
 
-  const int N = p.N, S = p.S, T = p.T;
-  int* s_len = smem_dyn;           // [S] q_len
-  int* s_id = s_len + S;           // [S] slot
-  int* s_start = s_id + S;         // [S] first row
-  int* s_pos = s_start + S;        // [S] rank of the first row inside its (class, slot) bin
-  int* s_tile = s_pos + S;         // [S] rank of the first tile inside its slot's tiles
-  int* s_key = s_tile + S;         // [S] (class, slot) key, -1 if the sequence is inactive; bits 24..28:
+  const int N = p.N, Scap = p.S, T = p.T;
+  int* s_len = smem_dyn;              // [S] q_len
+  int* s_id = s_len + Scap;           // [S] slot
+  int* s_start = s_id + Scap;         // [S] first row
+  int* s_pos = s_start + Scap;        // [S] rank of the first row inside its (class, slot) bin
+  int* s_tile = s_pos + Scap;         // [S] rank of the first tile inside its slot's tiles
+  int* s_key = s_tile + Scap;         // [S] (class, slot) key, -1 if the sequence is inactive; bits 24..28:
                                    //     the last lane of its warp with the same key
-  int* cnt_tok = s_key + S;        // [2N] rows per (class, slot), then their first perm position
+  int* cnt_tok = s_key + Scap;     // [2N] rows per (class, slot), then their first perm position
   int* run_tok = cnt_tok + 2 * N;  // [2N] running position while ranking sequences
   int* cnt_tile = run_tok + 2 * N; // [N]  class-1 tiles per slot, then the first tile index
   int* dec_cnt = cnt_tile + N;     // [N+1] decode groups per slot, then the first group index
@@ -183,6 +184,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kLeadShift = 24, kKeyMask = (1 << kLeadShift) - 1;  // keys < 2N <= 4096
+  // the sequence count (from the device when a run-length pass wrote it)
+  const int S = p.S_dev ? min(max(*p.S_dev, 0), Scap) : Scap;
 
   // ---- load the sequences once; validation by block reductions
   for (int i = tid; i < 2 * N; i += kSegThreads) run_tok[i] = 0;
@@ -382,14 +385,89 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   }
 }
 
+// Dispatched rows of an MoE layer -> the builder's sequences.  After routing,
+// the rows of each expert are contiguous and, inside an expert, the rows of
+// one sequence are contiguous; a maximal run of rows with the same (expert,
+// sequence, adapter) becomes one sequence whose slot is the expert's copy of
+// the adapter (1 + e * A + (a - 1); adapter 0 is the base model) and whose
+// length is the run's length (xLLM PR #2014, "Not in this PR": the fused MoE
+// expert LoRA delta by a grouped GEMM).  So a run of a prompt chunk's tokens
+// routed to one expert is a dense tile on the tensor path exactly when enough
+// of the chunk's own tokens chose that expert; other sequences never change
+// it.  One CTA: a block scan of the run-start flags.  An expert or adapter id
+// out of range gives the run slot N, which the builder reports as
+// LORA_ERR_SLOT; more runs than the capacity give no runs, which the builder
+// reports as LORA_ERR_META.
+struct MoeRunParams {
+  const int32_t* row_expert;
+  const int32_t* row_adapter;
+  const int32_t* row_seq;
+  int T, E, A, N, cap;
+  int32_t* run_ids;
+  int32_t* run_lens;
+  int32_t* run_starts;  // scratch (the builder rewrites this array as its seq_start)
+  int32_t* run_count;
+};
+
+constexpr int kRunThreads = 1024;
+
+__global__ void __launch_bounds__(kRunThreads, 1) moe_runs_kernel(MoeRunParams p) {
+  __shared__ int sums[33];
+  pdl_wait();  // the previous kernel's results are visible from here on
+  int carry = 0;
+  for (int b = 0; b < p.T; b += kRunThreads) {
+    const int r = b + threadIdx.x;
+    int flag = 0, slot = 0;
+    if (r < p.T) {
+      const int e = p.row_expert[r], sq = p.row_seq[r], a = p.row_adapter[r];
+      flag = r == 0 || e != p.row_expert[r - 1] || sq != p.row_seq[r - 1] || a != p.row_adapter[r - 1];
+      slot = (e < 0 || e >= p.E || a < 0 || a > p.A) ? p.N : (a == 0 ? 0 : 1 + e * p.A + (a - 1));
+    }
+    int tot;
+    const int idx = carry + block_exclusive_scan(flag, sums, tot);
+    if (flag && idx < p.cap) {
+      p.run_ids[idx] = slot;
+      p.run_starts[idx] = r;
+    }
+    carry += tot;
+  }
+  __syncthreads();  // every run start is written (and visible to the block)
+  const int n = carry <= p.cap ? carry : 0;
+  for (int i = threadIdx.x; i < n; i += kRunThreads)
+    p.run_lens[i] = (i + 1 < n ? p.run_starts[i + 1] : p.T) - p.run_starts[i];
+  if (threadIdx.x == 0) *p.run_count = n;
+  pdl_launch_next();  // the builder may be scheduled; it waits for this grid
+}
+
 }  // namespace
 
+int launch_moe_runs(lora_segments* seg, const int32_t* row_expert, const int32_t* row_adapter,
+                    const int32_t* row_seq, int T, int E, int A, cudaStream_t st) {
+  MoeRunParams p;
+  p.row_expert = row_expert;
+  p.row_adapter = row_adapter;
+  p.row_seq = row_seq;
+  p.T = T;
+  p.E = E;
+  p.A = A;
+  p.N = seg->N;
+  p.cap = T < seg->max_seqs ? T : seg->max_seqs;
+  p.run_ids = seg->run_ids;
+  p.run_lens = seg->run_lens;
+  p.run_starts = seg->seq_start;
+  p.run_count = seg->counts + 8;
+  const cudaError_t e = launch_pdl(moe_runs_kernel, dim3(1), dim3(kRunThreads), 0, st, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "moe_runs_kernel launch");
+}
+
 int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens, int S, int T,
-                     cudaStream_t st) {
+                     cudaStream_t st, const int32_t* S_dev) {
   SegParams p;
   p.ids = ids;
   p.lens = lens;
   p.S = S;
+  p.S_dev = S_dev;
   p.T = T;
   p.N = seg->N;
   p.status = seg->status;
@@ -416,7 +494,7 @@ using namespace lora;
 namespace {
 
 struct SegLayout {
-  size_t status, counts, seq_start, slot, perm, seg_off, dec_work, dec_rows, tc_work, total;
+  size_t status, counts, seq_start, slot, perm, seg_off, dec_work, dec_rows, tc_work, run_ids, run_lens, total;
   int cap_dec, cap_tc;
 };
 
@@ -438,6 +516,8 @@ bool seg_layout(int max_seqs, int max_tokens, int N, SegLayout* L) {
   L->dec_work = o; o = align256(o + 16 * (size_t)L->cap_dec);
   L->dec_rows = o; o = align256(o + 4 * (size_t)kDecGroup * L->cap_dec);
   L->tc_work = o; o = align256(o + 16 * (size_t)L->cap_tc);
+  L->run_ids = o; o = align256(o + 4 * (size_t)max_seqs);
+  L->run_lens = o; o = align256(o + 4 * (size_t)max_seqs);
   L->total = o;
   return true;
 }
@@ -479,6 +559,8 @@ int lora_segments_create(lora_segments** out, void* dev_ws, size_t ws_bytes, int
   s->dec_work = reinterpret_cast<int4*>(b + L.dec_work);
   s->dec_rows = reinterpret_cast<int32_t*>(b + L.dec_rows);
   s->tc_work = reinterpret_cast<int4*>(b + L.tc_work);
+  s->run_ids = reinterpret_cast<int32_t*>(b + L.run_ids);
+  s->run_lens = reinterpret_cast<int32_t*>(b + L.run_lens);
   *out = s;
   return LORA_OK;
 }
@@ -504,6 +586,39 @@ int lora_build_segments(lora_segments* seg, const int32_t* adapter_ids, const in
   seg->S = num_seqs;
   seg->T = num_tokens;
   return launch_seg_build(seg, adapter_ids, q_seq_lens, num_seqs, num_tokens, st);
+}
+
+int lora_moe_slot(int expert, int adapter, int num_adapters) {
+  return adapter == 0 ? 0 : 1 + expert * num_adapters + (adapter - 1);
+}
+
+int lora_build_segments_moe(lora_segments* seg, const int32_t* row_expert, const int32_t* row_adapter,
+                            const int32_t* row_seq, int num_rows, int num_experts, int num_adapters,
+                            lora_stream_t stream) {
+  if (!seg) return LORA_ERR_ARG;
+  if (num_rows < 0 || num_experts < 1 || num_adapters < 1) return LORA_ERR_SHAPE;
+  if ((long long)num_experts * num_adapters + 1 != seg->N) return LORA_ERR_SHAPE;
+  if (num_rows > seg->max_tokens) return LORA_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (num_rows == 0) {  // no dispatched rows: nothing to route, no kernel
+    seg->S = 0;
+    seg->T = 0;
+    if (cudaMemsetAsync(seg->counts, 0, 16, st) != cudaSuccess) return LORA_ERR_CUDA;
+    return cudaMemsetAsync(seg->status, 0, 4, st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+  }
+  if (!row_expert || !row_adapter || !row_seq) return LORA_ERR_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  if (dev != seg->device) return LORA_ERR_ARG;
+  // the runs are at most the rows and at most the capacity (more runs than
+  // max_seqs is a device-detected LORA_ERR_META): the builder's layout and
+  // the launchers' bounds take that many sequences
+  const int cap = num_rows < seg->max_seqs ? num_rows : seg->max_seqs;
+  seg->S = cap;
+  seg->T = num_rows;
+  const int r = launch_moe_runs(seg, row_expert, row_adapter, row_seq, num_rows, num_experts, num_adapters, st);
+  if (r != LORA_OK) return r;
+  return launch_seg_build(seg, seg->run_ids, seg->run_lens, cap, num_rows, st, seg->counts + 8);
 }
 
 int lora_segments_capacity(const lora_segments* seg, int* dec_work_cap, int* tc_work_cap) {

@@ -53,6 +53,8 @@ def load_library(path: str = LIB_PATH):
         "lora_segments_bytes": (SZ, [I, I, I]),
         "lora_segments_create": (I, [P, P, SZ, I, I, I]),
         "lora_build_segments": (I, [P, P, P, I, I, P]),
+        "lora_build_segments_moe": (I, [P, P, P, P, I, I, I, P]),
+        "lora_moe_slot": (I, [I, I, I]),
         "lora_segments_capacity": (I, [P, P, P]),
         "lora_segments_read": (I, [P, P, P, P, P, P, P, P]),
         "lora_segments_read_dec_rows": (I, [P, P, P]),
@@ -138,6 +140,17 @@ def lora_build_segments(seg: int, adapter_ids: int, q_seq_lens: int, num_seqs: i
                         stream: int = 0) -> None:
     _check(load_library().lora_build_segments(seg, adapter_ids, q_seq_lens, num_seqs, num_tokens, stream),
            "lora_build_segments")
+
+
+def lora_moe_slot(expert: int, adapter: int, num_adapters: int) -> int:
+    """Pool slot of adapter `adapter` (1..A; 0 = base) of expert `expert`."""
+    return int(load_library().lora_moe_slot(expert, adapter, num_adapters))
+
+
+def lora_build_segments_moe(seg: int, row_expert: int, row_adapter: int, row_seq: int, num_rows: int,
+                            num_experts: int, num_adapters: int, stream: int = 0) -> None:
+    _check(load_library().lora_build_segments_moe(seg, row_expert, row_adapter, row_seq, num_rows, num_experts,
+                                                  num_adapters, stream), "lora_build_segments_moe")
 
 
 def lora_segments_capacity(seg: int):
@@ -277,6 +290,17 @@ class LoraSegments:
         T = int(q_seq_lens.sum().item()) if num_tokens is None else int(num_tokens)
         lora_build_segments(self.handle, adapter_ids.data_ptr(), q_seq_lens.data_ptr(), S, T, _stream(stream))
         self.num_tokens = T
+
+    def build_moe(self, row_expert, row_adapter, row_seq, num_experts: int, num_adapters: int,
+                  stream=None) -> None:
+        """Dispatched MoE rows: int32 device tensors [num_rows] (expert, adapter, sequence of each row)."""
+        import torch
+        for t in (row_expert, row_adapter, row_seq):
+            assert t.dtype == torch.int32 and t.is_cuda
+        n = int(row_expert.numel())
+        lora_build_segments_moe(self.handle, row_expert.data_ptr(), row_adapter.data_ptr(), row_seq.data_ptr(), n,
+                                num_experts, num_adapters, _stream(stream))
+        self.num_tokens = n
 
     def read(self, stream=None) -> dict:
         return lora_segments_read(self.handle, self.num_tokens, self.num_slots, _stream(stream))

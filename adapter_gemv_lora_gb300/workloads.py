@@ -38,6 +38,10 @@ __all__ = [
     "make_workload",
     "custom_workload",
     "CONFIG_NAMES",
+    "MoeProjection",
+    "MoeWorkload",
+    "MOE_CONFIG_NAMES",
+    "make_moe_workload",
 ]
 
 
@@ -295,3 +299,148 @@ def custom_workload(q_seq_lens: Sequence[int], adapter_ids: Sequence[int], d_in:
                                            np.asarray(alpha, dtype=np.float64).reshape(num_slots, L),
                                            int(q.sum()), max_rank, strength=strength))
     return wl
+
+
+# ---------------------------------------------------------------- MoE layers
+#
+# Expert LoRA of an MoE layer (xLLM PR #2014 lists the fused MoE expert LoRA
+# delta as the next step; its validation model is a 30B-A3B MoE with r=16,
+# alpha=32).  Every expert has its own factors per adapter.  Tokens choose
+# top_k distinct experts; the dispatched rows (one per (token, expert)) are
+# grouped by expert, tokens in order inside an expert, as an MoE layer lays
+# them out before its expert GEMMs.
+
+
+@dataclass
+class MoeProjection:
+    """One expert projection: factors per (expert, adapter, lane) and the
+    dispatched rows' activations and base outputs.
+
+    A[e][a][l] uint16 bf16 [rank[a][l], d_in] (None for adapter 0 or rank 0),
+    B[e][a][l] uint16 bf16 [lane_d_out[l], rank[a][l]]; rank and scale are per
+    adapter (shared by the experts); x [R, d_in] bf16 bits, y0 [R, D] float32.
+    """
+
+    name: str
+    d_in: int
+    lane_d_out: List[int]
+    rank: np.ndarray          # int32 [A + 1, L]
+    scale: np.ndarray         # float32 [A + 1, L]
+    A: list
+    B: list
+    x: np.ndarray
+    y0: np.ndarray
+    max_rank: int
+
+    @property
+    def num_lanes(self) -> int:
+        return len(self.lane_d_out)
+
+    @property
+    def D(self) -> int:
+        return int(sum(self.lane_d_out))
+
+
+@dataclass
+class MoeWorkload:
+    name: str
+    seq_lens: np.ndarray      # int32 [S] tokens per sequence
+    seq_adapter: np.ndarray   # int32 [S] adapter of each sequence (0 = base)
+    num_experts: int
+    num_adapters: int         # adapters 1..A
+    top_k: int
+    row_token: np.ndarray     # int32 [R] token of each dispatched row
+    row_expert: np.ndarray    # int32 [R]
+    row_seq: np.ndarray       # int32 [R]
+    row_adapter: np.ndarray   # int32 [R]
+    projections: List[MoeProjection] = field(default_factory=list)
+
+    @property
+    def R(self) -> int:
+        return int(self.row_expert.shape[0])
+
+    @property
+    def T(self) -> int:
+        return int(self.seq_lens.sum())
+
+
+MOE_CONFIG_NAMES = ["moe_decode", "moe_prefill"]
+
+
+def _draw_moe_projection(rng, name, d_in, lane_d_out, E, A, rank, alpha, R, max_rank) -> MoeProjection:
+    L = len(lane_d_out)
+    scale = np.zeros((A + 1, L), dtype=np.float32)
+    for a in range(1, A + 1):
+        for l in range(L):
+            if rank[a, l] > 0:
+                scale[a, l] = np.float32(alpha[a, l] / rank[a, l])
+    Af = [[[None] * L for _ in range(A + 1)] for _ in range(E)]
+    Bf = [[[None] * L for _ in range(A + 1)] for _ in range(E)]
+    for e in range(E):
+        for a in range(1, A + 1):
+            for l in range(L):
+                r = int(rank[a, l])
+                if r > 0:
+                    Af[e][a][l] = bf16_bits(rng.standard_normal((r, d_in), dtype=np.float32)
+                                            * np.float32(1.0 / np.sqrt(d_in)))
+                    Bf[e][a][l] = bf16_bits(rng.standard_normal((lane_d_out[l], r), dtype=np.float32)
+                                            * np.float32(1.0 / np.sqrt(r)))
+    D = int(sum(lane_d_out))
+    x = bf16_bits(rng.standard_normal((R, d_in), dtype=np.float32))
+    y0 = rng.standard_normal((R, D), dtype=np.float32)
+    return MoeProjection(name, d_in, list(lane_d_out), rank.astype(np.int32), scale, Af, Bf, x, y0, max_rank)
+
+
+def moe_workload(name, seq_lens, seq_adapter, num_experts, num_adapters, top_k, d_model, d_expert,
+                 rank_per_adapter, seed=0) -> MoeWorkload:
+    """Routing (top_k distinct experts per token, uniform), the dispatch order
+    (rows grouped by expert, tokens in order) and the expert projections
+    gate_up (d_model -> 2 x d_expert) and down (d_expert -> d_model)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    seq_adapter = np.asarray(seq_adapter, dtype=np.int32)
+    T = int(seq_lens.sum())
+    tok_seq = np.repeat(np.arange(seq_lens.shape[0], dtype=np.int32), seq_lens)
+    choice = np.stack([rng.choice(num_experts, size=top_k, replace=False) for _ in range(T)]).astype(np.int32)
+    tok = np.repeat(np.arange(T, dtype=np.int32), top_k)
+    exp = choice.reshape(-1)
+    order = np.lexsort((tok, exp))  # by expert, then token
+    row_token, row_expert = tok[order].astype(np.int32), exp[order].astype(np.int32)
+    row_seq = tok_seq[row_token]
+    row_adapter = seq_adapter[row_seq]
+    wl = MoeWorkload(name, seq_lens, seq_adapter, num_experts, num_adapters, top_k, row_token, row_expert,
+                     row_seq.astype(np.int32), row_adapter.astype(np.int32))
+    R = wl.R
+    rank = np.zeros((num_adapters + 1, 1), dtype=np.int32)
+    rank[1:, 0] = np.asarray(rank_per_adapter, dtype=np.int32)
+    rank2 = np.repeat(rank, 2, axis=1)
+    wl.projections.append(_draw_moe_projection(rng, "experts.gate_up_proj", d_model, [d_expert, d_expert],
+                                               num_experts, num_adapters, rank2, 2.0 * rank2, R,
+                                               int(rank.max())))
+    wl.projections.append(_draw_moe_projection(rng, "experts.down_proj", d_expert, [d_model], num_experts,
+                                               num_adapters, rank, 2.0 * rank, R, int(rank.max())))
+    return wl
+
+
+def make_moe_workload(name: str, seed: int = 0) -> MoeWorkload:
+    """Expert-LoRA workloads on a 30B-A3B-class MoE layer (128 experts, top 8,
+    d_model 2048, expert width 768), 8 adapters of rank 16 (alpha 32):
+
+    moe_decode   256 single-token sequences (2048 dispatched rows), 20 % (51)
+                 base sequences by permutation, the rest uniform over 1..8
+    moe_prefill  2 prompt chunks of 1024 tokens (16384 dispatched rows; a
+                 chunk's tokens that chose one expert, about 64 rows, sit on
+                 both sides of the tensor-path threshold), adapters 1 and 2
+    """
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    E, A, k = 128, 8, 8
+    if name == "moe_decode":
+        S = 256
+        lens = np.ones(S, dtype=np.int32)
+        ids = _base_rows_by_permutation(rng, S, 51, A + 1)
+    elif name == "moe_prefill":
+        lens = np.array([1024, 1024], dtype=np.int32)
+        ids = np.array([1, 2], dtype=np.int32)
+    else:
+        raise KeyError(name)
+    return moe_workload(name, lens, ids, E, A, k, 2048, 768, [16] * A, seed=seed)

@@ -234,6 +234,52 @@ def setup_device_workload(wl, dev):
     return projs, seg, ids, lens
 
 
+def setup_device_moe(wl, dev):
+    """Pools (every expert's copy of every adapter at lora_moe_slot), the
+    dispatched rows' x / y and the routing tensors of an MoE workload."""
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    N = 1 + wl.num_experts * wl.num_adapters
+    projs = []
+    for mp in wl.projections:
+        pool = LD.LoraPool(N, mp.max_rank, mp.d_in, mp.lane_d_out, wl.R, device=dev)
+        for e in range(wl.num_experts):
+            for a in range(1, wl.num_adapters + 1):
+                k = LD.lora_moe_slot(e, a, wl.num_adapters)
+                for l in range(mp.num_lanes):
+                    if mp.rank[a, l] > 0:
+                        A = torch.from_numpy(mp.A[e][a][l].view(np.int16)).to(dev)
+                        B = torch.from_numpy(mp.B[e][a][l].view(np.int16)).to(dev)
+                        pool.load(k, l, A, B, float(mp.scale[a, l]))
+            torch.cuda.synchronize()
+        x = torch.from_numpy(mp.x.view(np.int16)).to(dev)
+        y0 = torch.from_numpy(mp.y0).to(dev)
+        projs.append({"proj": mp, "pool": pool, "x": x, "y0": y0, "y": y0.clone()})
+    seg = LD.LoraSegments(min(wl.R, 4096), wl.R, N, device=dev)
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v, dtype=np.int32)).to(dev)
+    routing = (t(wl.row_expert), t(wl.row_adapter), t(wl.row_seq))
+    return projs, seg, routing
+
+
+def moe_units(wl):
+    """Algorithmic bytes and flops of one MoE step: every dispatched row with
+    an adapter moves its x (2 d_in) and its y (8 D) once; every present
+    (expert, adapter, lane) its factors once (2 r (d_in + d_out))."""
+    total, flops = 0, 0
+    act = wl.row_adapter != 0
+    pairs = np.unique(np.stack([wl.row_expert[act], wl.row_adapter[act]], axis=1), axis=0) if act.any() else []
+    for mp in wl.projections:
+        n = int(act.sum())
+        total += n * (2 * mp.d_in + 8 * mp.D)
+        for e, a in pairs:
+            n_ea = int(((wl.row_expert == e) & (wl.row_adapter == a)).sum())
+            for l in range(mp.num_lanes):
+                r = int(mp.rank[a, l])
+                total += 2 * r * (mp.d_in + mp.lane_d_out[l])
+                flops += n_ea * 2 * r * (mp.d_in + mp.lane_d_out[l])
+    return total, flops
+
+
 def time_ours(wl, steps, warmup, dev, sampler_index):
     """Device times of one workload's step.
 
@@ -248,8 +294,14 @@ def time_ours(wl, steps, warmup, dev, sampler_index):
     y is restored and L2 flushed before every timed replay, outside the events."""
     import torch
     from adapter_gemv_lora_gb300 import lora_delta as LD
-    projs, seg, ids, lens = setup_device_workload(wl, dev)
-    T = wl.T
+    moe = isinstance(wl, W.MoeWorkload)
+    if moe:
+        projs, seg, routing = setup_device_moe(wl, dev)
+        ids = lens = None
+        T = wl.R
+    else:
+        projs, seg, ids, lens = setup_device_workload(wl, dev)
+        T = wl.T
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     n_ev = 2 + len(STAGES) * len(projs)
@@ -260,8 +312,13 @@ def time_ours(wl, steps, warmup, dev, sampler_index):
         flush.fill_(1)
 
     def build():
-        LD.lora_build_segments(seg.handle, ids.data_ptr(), lens.data_ptr(), wl.S, T,
-                               torch.cuda.current_stream().cuda_stream)
+        if moe:
+            LD.lora_build_segments_moe(seg.handle, routing[0].data_ptr(), routing[1].data_ptr(),
+                                       routing[2].data_ptr(), T, wl.num_experts, wl.num_adapters,
+                                       torch.cuda.current_stream().cuda_stream)
+        else:
+            LD.lora_build_segments(seg.handle, ids.data_ptr(), lens.data_ptr(), wl.S, T,
+                                   torch.cuda.current_stream().cuda_stream)
 
     def applies():
         for pr in projs:
@@ -654,6 +711,24 @@ def per_workload_summary(args, dev, hbm_peak, bf16_peak, headline):
             rec["cpu_oracle"] = {"threads_1": cpu_oracle_rates(wl, 1, args.cpu_seconds_detail),
                                  "threads_all": cpu_oracle_rates(wl, 0, args.cpu_seconds_detail)}
         out[name] = rec
+    for name in W.MOE_CONFIG_NAMES:
+        # MoE expert LoRA (not one of the five reference configurations)
+        wl = W.make_moe_workload(name, seed=args.seed)
+        res, ctx = time_ours(wl, args.steps, args.warmup, dev, 0)
+        del ctx
+        torch.cuda.empty_cache()
+        b, f = moe_units(wl)
+        sm, am = res["step_ms"], res["apply_ms"]
+        out[name] = {"dispatched_rows": wl.R, "tokens": wl.T, "experts": wl.num_experts, "top_k": wl.top_k,
+                     "adapters": wl.num_adapters,
+                     "projections": [{"name": p.name, "d_in": p.d_in, "lanes": p.lane_d_out} for p in wl.projections],
+                     "ms_per_step": round(sm, 5), "apply_ms": round(am, 5), "seg_build_ms": round(res["seg_ms"], 5),
+                     "rows_per_s": round(wl.R / (sm * 1e-3), 1), "alg_bytes": int(b), "flops": int(f),
+                     "frac_hbm_step": round(b / (sm * 1e-3) / 1e9 / hbm_peak, 4),
+                     "frac_hbm_apply": round(b / (am * 1e-3) / 1e9 / hbm_peak, 4),
+                     "stage_ms": [{k: round(v, 5) for k, v in st.items()} for st in res["stage_ms"]],
+                     "clocks": res["clocks"], "note": "expert LoRA on dispatched rows (MoE layer); not one of the "
+                                                      "five reference configurations"}
     return out
 
 

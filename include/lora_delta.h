@@ -158,6 +158,35 @@ int lora_segments_create(lora_segments** out, void* dev_ws, size_t ws_bytes, int
 int lora_build_segments(lora_segments* seg, const int32_t* adapter_ids, const int32_t* q_seq_lens,
                         int num_seqs, int num_tokens, lora_stream_t stream);
 
+/* ------------------------------------------------------- MoE expert LoRA --
+ * The delta of an MoE layer's expert projections, where every expert has its
+ * own LoRA factors per adapter (xLLM PR #2014, "Not in this PR": the fused MoE
+ * expert LoRA delta by a grouped GEMM; TensorFold PR #47 also names the
+ * shared expert's w2).  After routing, the layer's dispatched rows (one per
+ * (token, chosen expert)) are grouped by expert, and inside an expert the rows
+ * of one sequence are contiguous.  One pool holds every expert's copy of every
+ * adapter: adapter k (1..A) of expert e (0..E-1) sits in slot
+ * lora_moe_slot(e, k, A) = 1 + e * A + (k - 1), so num_slots = 1 + E * A
+ * (<= LORA_MAX_SLOTS); adapter 0 is the base model.  lora_build_segments_moe
+ * turns the dispatched rows into the builder's sequences: each maximal run of
+ * rows with the same (expert, sequence, adapter) is one sequence of that
+ * expert's adapter slot, so the run takes the tensor path when it has at least
+ * LORA_TC_MIN_QLEN rows (a prompt chunk's tokens that chose one expert).  The
+ * ordinary lora_apply_shrink_expand then adds the delta to the dispatched
+ * rows' fp32 outputs (x, y: [num_rows] dispatched rows).
+ *   row_expert[num_rows], row_adapter[num_rows], row_seq[num_rows]: device
+ *     int32; row_seq only delimits runs (any id, equal for a sequence's rows).
+ * The segments must have num_slots = 1 + E * A, max_tokens >= num_rows and
+ * max_seqs >= the number of runs.  Two kernels (a run-length pass, then the
+ * builder) on `stream`.  Device-detected errors: LORA_ERR_SLOT (an expert id
+ * outside [0, E) or an adapter id outside [0, A]), LORA_ERR_META (more runs
+ * than max_seqs); host errors: LORA_ERR_ARG, LORA_ERR_SHAPE.
+ * num_rows = 0 is a no-op step (no kernel). */
+int lora_moe_slot(int expert, int adapter, int num_adapters);
+int lora_build_segments_moe(lora_segments* seg, const int32_t* row_expert, const int32_t* row_adapter,
+                            const int32_t* row_seq, int num_rows, int num_experts, int num_adapters,
+                            lora_stream_t stream);
+
 /* Capacities of the work lists of this descriptor (host, no GPU work). */
 int lora_segments_capacity(const lora_segments* seg, int* dec_work_cap, int* tc_work_cap);
 

@@ -148,3 +148,68 @@ def delta(proj, slot: np.ndarray, rows: Optional[Sequence[int]] = None, num_thre
                      _ptr(x), x.shape[1], _ptr(slot), _ptr(y0), y0.shape[1],
                      _ptr(rows), n, _ptr(y_ref), _ptr(dl), int(num_threads))
     return y_ref[:n], dl[:n]
+
+
+# ------------------------------------------------------------------ MoE layers
+#
+# Expert LoRA of an MoE layer: each dispatched row (token, chosen expert) takes
+# the delta of its expert's copy of its sequence's adapter.  The library's
+# routing rule (its header, the MoE section): a maximal run of dispatched rows
+# with the same (expert, sequence, adapter) is one sequence of the builder,
+# whose slot is 1 + expert * A + (adapter - 1) (0 for the base model).  Written
+# out here independently, as plain loops.
+
+def moe_slot(expert: int, adapter: int, num_adapters: int) -> int:
+    """Slot of an expert's copy of an adapter (0 for the base model)."""
+    if adapter == 0:
+        return 0
+    return 1 + expert * num_adapters + (adapter - 1)
+
+
+def moe_runs(row_expert, row_adapter, row_seq, num_experts: int, num_adapters: int):
+    """(ids, lens) of the runs of equal (expert, sequence, adapter), in row
+    order; an expert or adapter id out of range gives slot 1 + E * A (out of
+    the pool's range)."""
+    ids, lens = [], []
+    prev = None
+    n_slots = 1 + num_experts * num_adapters
+    for e, a, s in zip(map(int, row_expert), map(int, row_adapter), map(int, row_seq)):
+        key = (e, s, a)
+        if key != prev:
+            ok = 0 <= e < num_experts and 0 <= a <= num_adapters
+            ids.append(moe_slot(e, a, num_adapters) if ok else n_slots)
+            lens.append(0)
+            prev = key
+        lens[-1] += 1
+    return np.asarray(ids, dtype=np.int32), np.asarray(lens, dtype=np.int32)
+
+
+class _SlotProjection:
+    """A projection view over slots 0..N-1 (the attributes delta() reads)."""
+
+    def __init__(self, d_in, lane_d_out, rank, scale, A, B, x, y0, max_rank):
+        self.d_in, self.lane_d_out = d_in, list(lane_d_out)
+        self.rank, self.scale, self.A, self.B = rank, scale, A, B
+        self.x, self.y0, self.max_rank = x, y0, max_rank
+
+    @property
+    def num_lanes(self):
+        return len(self.lane_d_out)
+
+
+def moe_projection(mproj, num_experts: int, num_adapters: int):
+    """The expert projection as a projection over slots 1 + E * A (slot of
+    (e, a) by moe_slot), for delta()."""
+    N, L = 1 + num_experts * num_adapters, mproj.num_lanes
+    rank = np.zeros((N, L), dtype=np.int32)
+    scale = np.zeros((N, L), dtype=np.float32)
+    A = [[None] * L for _ in range(N)]
+    B = [[None] * L for _ in range(N)]
+    for e in range(num_experts):
+        for a in range(1, num_adapters + 1):
+            k = moe_slot(e, a, num_adapters)
+            for l in range(L):
+                rank[k, l] = mproj.rank[a, l]
+                scale[k, l] = mproj.scale[a, l]
+                A[k][l], B[k][l] = mproj.A[e][a][l], mproj.B[e][a][l]
+    return _SlotProjection(mproj.d_in, mproj.lane_d_out, rank, scale, A, B, mproj.x, mproj.y0, mproj.max_rank)

@@ -319,3 +319,51 @@ def test_workload_configs_metadata(oracle_mod):
     for name in W.CONFIG_NAMES:
         wl = W.make_workload(name, draw_xy=False)
         _check_meta(oracle_mod, wl.adapter_ids, wl.q_seq_lens, wl.T, wl.num_slots)
+
+
+# ------------------------------------------------------------------ MoE layers
+
+def test_moe_slot_follows_the_documented_rule():
+    # adapter k (1..A) of expert e sits in slot 1 + e * A + (k - 1); adapter 0 is the base model
+    import oracle
+    assert oracle.moe_slot(0, 1, 8) == 1
+    assert oracle.moe_slot(3, 2, 8) == 26
+    assert oracle.moe_slot(127, 8, 8) == 1024
+    assert oracle.moe_slot(5, 0, 8) == 0
+
+
+def test_moe_runs_hand_example():
+    # rows grouped by expert; a run is a maximal stretch of equal (expert, sequence, adapter)
+    import oracle
+    e = [0, 0, 0, 1, 1, 2, 2]
+    s = [5, 5, 6, 5, 5, 6, 7]
+    a = [1, 1, 2, 1, 1, 0, 0]
+    ids, lens = oracle.moe_runs(e, a, s, 3, 8)
+    assert ids.tolist() == [1, 2, 9, 0, 0]
+    assert lens.tolist() == [2, 1, 2, 1, 1]
+    # an expert id out of range gets slot 1 + E * A (outside the pool)
+    ids, _ = oracle.moe_runs([0, 3], [1, 1], [0, 0], 3, 8)
+    assert ids.tolist() == [1, 25]
+
+
+def test_moe_delta_brute_force(oracle_mod):
+    # the oracle's slot view of an MoE projection against the delta written out
+    # per dispatched row: y0 + scale * B[e][a] @ (A[e][a] @ x)
+    from adapter_gemv_lora_gb300 import workloads as W
+    wl = W.moe_workload("t", [3, 1, 2], [1, 0, 2], num_experts=4, num_adapters=2, top_k=2, d_model=64,
+                        d_expert=64, rank_per_adapter=[3, 5], seed=4)
+    for mp in wl.projections:
+        ids, lens = oracle_mod.moe_runs(wl.row_expert, wl.row_adapter, wl.row_seq, 4, 2)
+        slot = np.repeat(ids, lens)
+        _, d = oracle_mod.delta(oracle_mod.moe_projection(mp, 4, 2), slot)
+        xf = W.bf16_bits_to_f32(mp.x).astype(np.float64)
+        off = np.concatenate([[0], np.cumsum(mp.lane_d_out)])
+        for r in range(wl.R):
+            e, a = int(wl.row_expert[r]), int(wl.row_adapter[r])
+            for l in range(mp.num_lanes):
+                ref = np.zeros(mp.lane_d_out[l])
+                if a > 0:
+                    Af = W.bf16_bits_to_f32(mp.A[e][a][l]).astype(np.float64)
+                    Bf = W.bf16_bits_to_f32(mp.B[e][a][l]).astype(np.float64)
+                    ref = float(mp.scale[a, l]) * (Bf @ (Af @ xf[r]))
+                np.testing.assert_allclose(d[r, off[l]:off[l + 1]], ref, rtol=1e-12, atol=1e-12)

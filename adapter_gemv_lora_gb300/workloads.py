@@ -42,6 +42,7 @@ __all__ = [
     "MoeWorkload",
     "MOE_CONFIG_NAMES",
     "make_moe_workload",
+    "projection_weight",
 ]
 
 
@@ -299,6 +300,16 @@ def custom_workload(q_seq_lens: Sequence[int], adapter_ids: Sequence[int], d_in:
                                            np.asarray(alpha, dtype=np.float64).reshape(num_slots, L),
                                            int(q.sum()), max_rank, strength=strength))
     return wl
+
+
+def projection_weight(proj, seed: int = 1) -> np.ndarray:
+    """The base projection's weight for the fused form, as a linear layer
+    stores it: bf16 bits [D][d_in] (output feature, input feature), the lanes
+    stacked in lane order, drawn N(0, 1/d_in) from its own PCG64 stream (so the
+    projection's other tensors stay as they were)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    w = rng.standard_normal((proj.D, proj.d_in), dtype=np.float32) * np.float32(1.0 / np.sqrt(proj.d_in))
+    return bf16_bits(w)
 
 
 # ---------------------------------------------------------------- MoE layers

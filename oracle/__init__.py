@@ -46,6 +46,9 @@ def _load():
         lib.oracle_delta.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P, P, P, P, P, P,
                                      P, i64, P, P, i64, P, i64, P, P, ctypes.c_int]
         lib.oracle_delta.restype = None
+        lib.oracle_base_product.argtypes = [ctypes.c_int, ctypes.c_int, P, i64, P, i64, P, i64, P, P,
+                                            ctypes.c_int]
+        lib.oracle_base_product.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -148,6 +151,36 @@ def delta(proj, slot: np.ndarray, rows: Optional[Sequence[int]] = None, num_thre
                      _ptr(x), x.shape[1], _ptr(slot), _ptr(y0), y0.shape[1],
                      _ptr(rows), n, _ptr(y_ref), _ptr(dl), int(num_threads))
     return y_ref[:n], dl[:n]
+
+
+def base_product(W: np.ndarray, x: np.ndarray, rows: Optional[Sequence[int]] = None, num_threads: int = 0):
+    """(base, abs_base) in float64 for the listed rows: base = x @ W^T over bf16
+    values (W is [D][d_in] bf16 bits, x is [T][d_in] bf16 bits), abs_base the
+    sum of the products' magnitudes.  Arrays of shape [len(rows), D]."""
+    lib = _load()
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    D, d_in = W.shape
+    assert x.shape[1] >= d_in
+    if rows is None:
+        rows = np.arange(x.shape[0], dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = int(rows.shape[0])
+    base = np.zeros((max(n, 1), D), dtype=np.float64)
+    mag = np.zeros((max(n, 1), D), dtype=np.float64)
+    lib.oracle_base_product(d_in, D, _ptr(W), W.shape[1], _ptr(x), x.shape[1], _ptr(rows), n,
+                            _ptr(base), _ptr(mag), int(num_threads))
+    return base[:n], mag[:n]
+
+
+def fused_projection(proj, W: np.ndarray, slot: np.ndarray, rows: Optional[Sequence[int]] = None,
+                     num_threads: int = 0, _flat=None):
+    """The projection with the delta in its output, float64, for the listed
+    rows: (y, delta, abs_base) with y = x @ W^T + delta (slot-0 rows: the
+    base product alone; y0 plays no part)."""
+    base, mag = base_product(W, proj.x, rows, num_threads)
+    _, dl = delta(proj, slot, rows, num_threads, _flat=_flat)
+    return base + dl, dl, mag
 
 
 # ------------------------------------------------------------------ MoE layers

@@ -243,6 +243,44 @@ void oracle_delta(int d_in, int L, const int32_t* d_out, int N,
   }
 }
 
+// The base projection the delta is added to, in double precision, for the
+// rows listed in rows[n_rows]:
+//     base[q][c]     = sum_j W[c][j] * x[t][j]      (j ascending), t = rows[q]
+//     abs_base[q][c] = sum_j |W[c][j] * x[t][j]|
+// W is the projection's weight as a linear layer stores it, [D][ldw] bf16
+// (output feature c, input feature j; the fused lanes stacked in lane order),
+// x is [T][ldx] bf16.  The delta "is added to the fp32 partial sum" of this
+// product (TensorFold PR #47, the paragraph on the delta); in the fused form a
+// row's output is base + delta, and a slot-0 row's output is the base alone
+// (xLLM PR #2014, the LoRARowParallelLinear item: the base's own output
+// carries the delta partial sum).  abs_base is the magnitude that bounds the
+// rounding error of any float32 evaluation of the same sum.
+void oracle_base_product(int d_in, int D, const uint16_t* W, int64_t ldw,
+                         const uint16_t* x, int64_t ldx,
+                         const int64_t* rows, int64_t n_rows,
+                         double* base, double* abs_base, int num_threads) {
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t q = 0; q < n_rows; ++q) {
+    const int64_t t = rows[q];
+    std::vector<double> xt(d_in);
+    for (int j = 0; j < d_in; ++j) xt[j] = bf16_to_double(x[t * ldx + j]);
+    for (int c = 0; c < D; ++c) {
+      const uint16_t* w = W + static_cast<int64_t>(c) * ldw;
+      double acc = 0.0, mag = 0.0;
+      for (int j = 0; j < d_in; ++j) {
+        const double p = bf16_to_double(w[j]) * xt[j];
+        acc += p;
+        mag += p < 0 ? -p : p;
+      }
+      base[q * D + c] = acc;
+      abs_base[q * D + c] = mag;
+    }
+  }
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -367,3 +367,78 @@ def test_moe_delta_brute_force(oracle_mod):
                     Bf = W.bf16_bits_to_f32(mp.B[e][a][l]).astype(np.float64)
                     ref = float(mp.scale[a, l]) * (Bf @ (Af @ xf[r]))
                 np.testing.assert_allclose(d[r, off[l]:off[l + 1]], ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ base projection
+# The fused form writes x @ W^T + delta (the delta is added to the projection's
+# fp32 partial sum: TensorFold PR #47, the paragraph on the delta).
+
+
+def test_base_product_permutation_slice_is_a_gather(oracle_mod):
+    # W[c][j] = 1 iff j == pi(c): the product picks x[t][pi(c)] exactly.
+    rng = np.random.default_rng(5)
+    d_in, D, T = 96, 64, 7
+    pi = rng.permutation(d_in)[:D]
+    w = np.zeros((D, d_in), dtype=np.float32)
+    w[np.arange(D), pi] = 1.0
+    x = W.bf16_bits(rng.standard_normal((T, d_in)).astype(np.float32))
+    base, mag = oracle_mod.base_product(W.bf16_bits(w), x)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    assert np.array_equal(base, xf[:, pi])
+    assert np.array_equal(mag, np.abs(xf[:, pi]))
+    # reading W transposed (column c of W as the weights of output c) gathers
+    # x[t][j] at the j whose pi(j) == c instead: a different matrix here
+    wt_gather = np.zeros((T, D))
+    for c in range(D):
+        hit = np.nonzero(pi == c)[0]
+        if hit.size:
+            wt_gather[:, c] = xf[:, hit[0]]
+    assert not np.array_equal(base, wt_gather)
+
+
+def test_base_product_against_exact_rationals(oracle_mod):
+    rng = np.random.default_rng(11)
+    d_in, D, T = 40, 24, 5
+    w = rng.standard_normal((D, d_in)).astype(np.float32)
+    x = rng.standard_normal((T, d_in)).astype(np.float32)
+    wb, xb = W.bf16_bits(w), W.bf16_bits(x)
+    base, mag = oracle_mod.base_product(wb, xb, rows=[4, 0, 2])
+    wf = W.bf16_bits_to_f32(wb)
+    xf = W.bf16_bits_to_f32(xb)
+    for q, t in enumerate([4, 0, 2]):
+        for c in range(D):
+            terms = [Fraction(float(wf[c, j])) * Fraction(float(xf[t, j])) for j in range(d_in)]
+            exact = sum(terms)
+            amag = sum(abs(v) for v in terms)
+            assert abs(base[q, c] - float(exact)) <= 1e-14 * float(amag)
+            assert abs(mag[q, c] - float(amag)) <= 1e-14 * float(amag)
+
+
+def test_fused_projection_closed_form(oracle_mod):
+    # W a permutation slice and a rank-1 adapter A = e_i, B = e_j with scale s:
+    # y[t][c] = x[t][pi(c)] + s * x[t][i] * [c == j] for adapter rows, and
+    # x[t][pi(c)] alone for base rows (y0 plays no part).
+    d_in, d_out, T = 64, 64, 6
+    i, j, s = 9, 40, -1.5
+    proj = _rank1_projection(d_in, d_out, i, j, s, T, seed=2)
+    pi = np.roll(np.arange(d_in), 7)[:d_out]
+    w = np.zeros((d_out, d_in), dtype=np.float32)
+    w[np.arange(d_out), pi] = 1.0
+    slot = np.array([1, 0, 1, 1, 0, 1], dtype=np.int32)
+    y, dl, _ = oracle_mod.fused_projection(proj, W.bf16_bits(w), slot)
+    xf = W.bf16_bits_to_f32(proj.x).astype(np.float64)
+    expect = xf[:, pi].copy()
+    expect[slot == 1, j] += s * xf[slot == 1, i]
+    assert np.array_equal(y, expect)
+    assert np.all(dl[slot == 0] == 0)
+
+
+def test_projection_weight_is_seeded_and_shaped():
+    wl = W.make_workload("tiny")
+    proj = wl.projections[0]
+    w1 = W.projection_weight(proj)
+    w2 = W.projection_weight(proj)
+    assert w1.shape == (proj.D, proj.d_in) and w1.dtype == np.uint16
+    assert np.array_equal(w1, w2)
+    wf = W.bf16_bits_to_f32(w1)
+    assert abs(float(wf.std()) * np.sqrt(proj.d_in) - 1.0) < 0.05

@@ -214,6 +214,72 @@ int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void
   return run_stage(pool->v, seg, x, y, ldx, ldy, stage, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+int check_fused(const lora_pool* pool, const lora_segments* seg, const void* W, int64_t ldw, const void* x,
+                const float* y, int64_t ldx, int64_t ldy) {
+  const int chk = check_apply(pool, seg, x, y, ldx, ldy);
+  if (chk != LORA_OK) return chk;
+  if (!W || (reinterpret_cast<uintptr_t>(W) & 15)) return LORA_ERR_ARG;
+  if (ldw < pool->v.d_in || (ldw % 8)) return LORA_ERR_ARG;
+  return LORA_OK;
+}
+
+int run_fused_stage(const lora_pool* pool, const lora_segments* seg, const void* W, int64_t ldw, const void* x,
+                    float* y, int64_t ldx, int64_t ldy, int stage, cudaStream_t st) {
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  switch (stage) {
+    case 1:
+      return pool_has_adapter(pool) ? launch_decode_rows(pool->v, seg, xb, ldx, st) : LORA_OK;
+    case 2:
+      return pool_has_adapter(pool) ? launch_tc_shrink_rows(pool->v, seg, xb, ldx, st) : LORA_OK;
+    case 3:
+      return launch_fused_projection(pool->v, seg, static_cast<const uint16_t*>(W), ldw, xb, ldx, y, ldy, st);
+    default:
+      return LORA_ERR_ARG;
+  }
+}
+}  // namespace
+
+int lora_apply_fused_projection(const lora_pool* pool, const lora_segments* seg, const void* W, int64_t ldw,
+                                const void* x, float* y, int64_t ldx, int64_t ldy, lora_stream_t stream) {
+  const int chk = check_fused(pool, seg, W, ldw, x, y, ldx, ldy);
+  if (chk != LORA_OK) return chk;
+  if (seg->T == 0) return LORA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  SideStream* side = pool_has_adapter(pool) ? side_stream() : nullptr;
+  if (!side) {
+    for (int stage = 1; stage <= 3; ++stage) {
+      const int r = run_fused_stage(pool, seg, W, ldw, x, y, ldx, ldy, stage, st);
+      if (r != LORA_OK) return r;
+    }
+    return LORA_OK;
+  }
+  // the decode shrink on the side stream, the tensor shrink on `stream`, joined
+  // before the GEMM (the two write disjoint rows of the per-row scratch)
+  std::lock_guard<std::mutex> lock(side->mu);
+  int r = cuda_status(cudaEventRecord(side->fork, st), "cudaEventRecord(fork)");
+  if (r == LORA_OK) r = cuda_status(cudaStreamWaitEvent(side->stream, side->fork, 0), "cudaStreamWaitEvent(fork)");
+  if (r != LORA_OK) return r;
+  const int rd = run_fused_stage(pool, seg, W, ldw, x, y, ldx, ldy, 1, side->stream);
+  const int rt = run_fused_stage(pool, seg, W, ldw, x, y, ldx, ldy, 2, st);
+  r = cuda_status(cudaEventRecord(side->join, side->stream), "cudaEventRecord(join)");
+  if (r == LORA_OK) r = cuda_status(cudaStreamWaitEvent(st, side->join, 0), "cudaStreamWaitEvent(join)");
+  if (rd != LORA_OK) return rd;
+  if (rt != LORA_OK) return rt;
+  if (r != LORA_OK) return r;
+  return run_fused_stage(pool, seg, W, ldw, x, y, ldx, ldy, 3, st);
+}
+
+int lora_fused_projection_stage(const lora_pool* pool, const lora_segments* seg, const void* W, int64_t ldw,
+                                const void* x, float* y, int64_t ldx, int64_t ldy, int stage,
+                                lora_stream_t stream) {
+  const int chk = check_fused(pool, seg, W, ldw, x, y, ldx, ldy);
+  if (chk != LORA_OK) return chk;
+  if (stage < 1 || stage > 3) return LORA_ERR_ARG;
+  if (seg->T == 0) return LORA_OK;
+  return run_fused_stage(pool, seg, W, ldw, x, y, ldx, ldy, stage, reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* lora_status_string(int status) {
   switch (status) {
     case LORA_OK: return "ok";

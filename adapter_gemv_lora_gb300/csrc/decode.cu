@@ -85,6 +85,7 @@ struct DfParams {
   int64_t ldx;
   float* y;
   int64_t ldy;
+  float* u_rows;  // row mode: scale * u of each row to [T][L][R16], no expand (y is not touched)
   int L, R16, nkb, npages;
   int parts;  // column parts per (group, lane), each its own unit (set on the device per step)
   int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES], bt_cols[LORA_MAX_LANES];
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
   {
     const int pairs = p.counts[2] * p.L;
     int parts = 1;
-    while (parts < 4 && pairs * parts * 2 <= (int)num_clusters_x()) parts *= 2;
+    while (!p.u_rows && parts < 4 && pairs * parts * 2 <= (int)num_clusters_x()) parts *= 2;
     p.parts = parts;
   }
   const int n_units = p.counts[2] * p.L * p.parts;
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
             }
           }
         }
-        for (int c0 = U.c0; c0 < U.c1 && ok; c0 += kDfCols) {
+        for (int c0 = U.c0; c0 < U.c1 && ok && !p.u_rows; c0 += kDfCols) {
           const int ec = min(kDfCols, U.c1 - c0);
           const int nbox = (ec + U.bi - 1) / U.bi;
           for (int rb = 0; rb < U.r && ok; rb += kDfRanksPerPage) {
@@ -560,6 +561,19 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
       }
       ++uj;
       named_bar_sync(1, kDfCompute);  // u complete
+      if (p.u_rows) {  // row mode: scale * u of the group's rows, written once (by CTA 0)
+        if (ok && cta == 0) {
+          const float sc = p.scale_tab[U.k * p.L + U.l];
+#pragma unroll
+          for (int g = 0; g < kDecGroup; ++g) {
+            if (g < U.nrows) {
+              float* dst = p.u_rows + ((size_t)U.row[g] * p.L + U.l) * p.R16;
+              for (int i = t; i < U.r16; i += kDfCompute) dst[i] = sc * us[i * kDecGroup + g];
+            }
+          }
+        }
+        continue;
+      }
       // ---- expand of this CTA's columns: thread tile rtile rows x 4 columns
       const float sc = p.scale_tab[U.k * p.L + U.l];
       // this thread's columns 4t..4t+3 of a chunk sit in TMA box 4t / bi of a B page
@@ -695,10 +709,11 @@ int max_active_clusters(int device, int ncta, size_t smem) {
 
 }  // namespace
 
-int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx, float* y,
-                  int64_t ldy, cudaStream_t st) {
-  // units: (group, lane) pairs, each in up to 4 column parts
-  const long long units = (long long)dec_group_bound(pool, seg) * pool.L * 4;
+namespace {
+int decode_impl(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx, float* y,
+                int64_t ldy, float* u_rows, cudaStream_t st) {
+  // units: (group, lane) pairs, each in up to 4 column parts (one in row mode)
+  const long long units = (long long)dec_group_bound(pool, seg) * pool.L * (u_rows ? 1 : 4);
   if (units <= 0) return LORA_OK;
   const int ncta = cluster_size(pool);
   const int npages = dec_pages(pool, ncta);
@@ -725,6 +740,7 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
   p.ldx = ldx;
   p.y = y;
   p.ldy = ldy;
+  p.u_rows = u_rows;
   p.L = pool.L;
   p.R16 = pool.R16;
   p.nkb = pool.d_in / 64;
@@ -747,6 +763,17 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
   const cudaError_t e = cudaLaunchKernelEx(&cfg, dec_fused_kernel, pool.tm_a, pool.tm_bt, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "dec_fused_kernel launch");
+}
+}  // namespace
+
+int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx, float* y,
+                  int64_t ldy, cudaStream_t st) {
+  return decode_impl(pool, seg, x, ldx, y, ldy, nullptr, st);
+}
+
+int launch_decode_rows(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                       cudaStream_t st) {
+  return decode_impl(pool, seg, x, ldx, nullptr, 0, pool.u_rows, st);
 }
 
 }  // namespace lora

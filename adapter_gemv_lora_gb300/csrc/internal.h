@@ -71,6 +71,8 @@ struct PoolView {
   uint16_t* u_fmt = nullptr;          // [tiles][L][2][128*R16] per tensor tile: U as bf16 hi then lo,
                                       // K-major core-matrix layout of the tile's own rank, ready for the expand
   int32_t* tile_cnt = nullptr;        // [tiles] K-range CTAs of a tile that finished (0 between calls)
+  float* u_rows = nullptr;            // [max_tokens][L][R16] per row scale * u (the fused projection's
+                                      // rank-space input; written by the shrinks run in their row mode)
   TmapSized tm_a;                     // A, 3-D {d_in, R16, N}, box {64, 16<<s, 1}, 128-byte swizzle
   TmapSized tm_bk;                    // Bk, 3-D {16, d_out, R16/16*N}, box {16, 128, 1<<s}, 32-byte swizzle
   TmapLanes tm_bt;                    // Bt, 3-D {d_out, R16, N}, box {min(256, d_out), 16, 1}, no swizzle
@@ -162,6 +164,16 @@ int launch_decode(const PoolView& pool, const lora_segments* seg, const uint16_t
                   int64_t ldy, cudaStream_t st);
 int launch_tc_shrink(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
                      cudaStream_t st);
+// Row mode of the two shrinks: scale * u of every active row goes to
+// pool.u_rows (fp32) and nothing else is written (no expand, no y access).
+int launch_decode_rows(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                       cudaStream_t st);
+int launch_tc_shrink_rows(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                          cudaStream_t st);
+// The fused projection y = x W^T + delta (one tcgen05 GEMM whose accumulator
+// also takes the expand), after the row-mode shrinks.
+int launch_fused_projection(const PoolView& pool, const lora_segments* seg, const uint16_t* W, int64_t ldw,
+                            const uint16_t* x, int64_t ldx, float* y, int64_t ldy, cudaStream_t st);
 int launch_tc_expand(const PoolView& pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st);
 
 }  // namespace lora

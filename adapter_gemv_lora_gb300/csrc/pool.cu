@@ -22,6 +22,8 @@
 //                                            bf16 hi and lo halves, in the
 //                                            layout the expand's MMA reads
 //   tile_cnt  int32 [tiles]                  per tile, K-range CTAs done
+//   u_rows    f32   [max_tokens][L][R16]     per row scale * u, the input of
+//                                            the fused projection's expand
 // The decode path needs no scratch: its rank-space vector stays on chip.
 // (tiles = max_tokens / 64 + 1, the most a build can make)
 #include <cuda_runtime.h>
@@ -61,7 +63,8 @@ __global__ void repack_kernel(const uint16_t* __restrict__ A, const uint16_t* __
 }
 
 struct PoolLayout {
-  size_t rank_tab, scale_tab, A[LORA_MAX_LANES], Bt[LORA_MAX_LANES], Bk[LORA_MAX_LANES], u_tc, u_fmt, tile_cnt, total;
+  size_t rank_tab, scale_tab, A[LORA_MAX_LANES], Bt[LORA_MAX_LANES], Bk[LORA_MAX_LANES], u_tc, u_fmt, tile_cnt,
+      u_rows, total;
   int R16;
 };
 
@@ -92,6 +95,7 @@ bool pool_layout(int N, int R, int d_in, int L, const int* d_out, int max_tokens
   P->u_tc = o; o = align1k(o + 4 * (size_t)kTcKSplit * tc_tile_cap(max_tokens) * L * R16 * kTcTile);
   P->u_fmt = o; o = align1k(o + 2 * (size_t)tc_tile_cap(max_tokens) * L * 2 * kTcTile * R16);
   P->tile_cnt = o; o = align1k(o + 4 * (size_t)tc_tile_cap(max_tokens));
+  P->u_rows = o; o = align1k(o + 4 * (size_t)max_tokens * L * R16);
   P->total = o;
   return true;
 }
@@ -162,6 +166,7 @@ int lora_pool_create(lora_pool** out, void* dev_mem, size_t bytes, int num_slots
   p->u_tc = reinterpret_cast<float*>(b + P.u_tc);
   p->u_fmt = reinterpret_cast<uint16_t*>(b + P.u_fmt);
   p->tile_cnt = reinterpret_cast<int32_t*>(b + P.tile_cnt);
+  p->u_rows = reinterpret_cast<float*>(b + P.u_rows);
   pp->h_rank.assign((size_t)num_slots * num_lanes, 0);
   std::memset(&p->tm_a, 0, sizeof(p->tm_a));
   std::memset(&p->tm_bk, 0, sizeof(p->tm_bk));

@@ -42,8 +42,10 @@ struct TcShrinkParams {
   const int32_t* counts;
   const int4* work;
   const int32_t* rank_tab;
+  const float* scale_tab;
   float* u_tc;
   uint16_t* u_fmt;
+  float* u_rows;  // row mode: scale * u per row [T][L][R16] instead of u_fmt
   int32_t* tile_cnt;
   int32_t* status;
   int L, R16, num_kb, ring_bytes, tmem_cols, tiles_cap;
@@ -318,6 +320,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                   acc = ks == 0 ? val : acc + val;
                 }
                 u[e] = valid ? acc : 0.f;
+              }
+              if (p.u_rows) {  // row mode: scale * u of this row, fp32
+                if (valid) {
+                  const float sc = p.scale_tab[k * p.L + l];
+                  float4* dst = reinterpret_cast<float4*>(p.u_rows + ((size_t)t * p.L + l) * p.R16 + c0 + 16 * q);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(sc * u[4 * e], sc * u[4 * e + 1], sc * u[4 * e + 2], sc * u[4 * e + 3]);
+                }
+                continue;
               }
 #pragma unroll
               for (int g = 0; g < 2; ++g) {
@@ -620,8 +632,9 @@ int tc_tile_bound(const lora_segments* seg) {
 
 }  // namespace
 
-int launch_tc_shrink(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
-                     cudaStream_t st) {
+namespace {
+int tc_shrink_impl(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx, float* u_rows,
+                   cudaStream_t st) {
   const int grid = tc_tile_bound(seg) * kTcKSplit;
   if (grid <= 0) return LORA_OK;
   CUtensorMap tm_x128, tm_x32;
@@ -640,6 +653,8 @@ int launch_tc_shrink(const PoolView& pool, const lora_segments* seg, const uint1
   p.counts = seg->counts;
   p.work = seg->tc_work;
   p.rank_tab = pool.rank_tab;
+  p.scale_tab = pool.scale_tab;
+  p.u_rows = u_rows;
   p.u_tc = pool.u_tc;
   p.u_fmt = pool.u_fmt;
   p.tile_cnt = pool.tile_cnt;
@@ -665,6 +680,17 @@ int launch_tc_shrink(const PoolView& pool, const lora_segments* seg, const uint1
   const cudaError_t e = launch_pdl(tc_shrink_kernel, dim3(grid), dim3(kTcThreads), smem, st, tm_x128, tm_x32, pool.tm_a, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "tc_shrink_kernel launch");
+}
+}  // namespace
+
+int launch_tc_shrink(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                     cudaStream_t st) {
+  return tc_shrink_impl(pool, seg, x, ldx, nullptr, st);
+}
+
+int launch_tc_shrink_rows(const PoolView& pool, const lora_segments* seg, const uint16_t* x, int64_t ldx,
+                          cudaStream_t st) {
+  return tc_shrink_impl(pool, seg, x, ldx, pool.u_rows, st);
 }
 
 int launch_tc_expand(const PoolView& pool, const lora_segments* seg, float* y, int64_t ldy, cudaStream_t st) {

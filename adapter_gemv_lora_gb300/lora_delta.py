@@ -64,6 +64,8 @@ def load_library(path: str = LIB_PATH):
         "lora_apply_shrink_expand": (I, [P, P, P, P, I64, I64, P]),
         "lora_apply_stage": (I, [P, P, P, P, I64, I64, I, P]),
         "lora_apply_shrink_expand_noalloc": (I, [P, P, P, P, I64, I64, P]),
+        "lora_apply_fused_projection": (I, [P, P, P, I64, P, P, I64, I64, P]),
+        "lora_fused_projection_stage": (I, [P, P, P, I64, P, P, I64, I64, I, P]),
         "lora_status_string": (ctypes.c_char_p, [I]),
         "lora_launch_count": (ctypes.c_uint64, []),
         "lora_last_error_string": (ctypes.c_char_p, []),
@@ -216,6 +218,18 @@ def lora_apply_stage(pool: int, seg: int, x: int, y: int, ldx: int, ldy: int, st
     _check(load_library().lora_apply_stage(pool, seg, x, y, ldx, ldy, stage, stream), "lora_apply_stage")
 
 
+def lora_apply_fused_projection(pool: int, seg: int, W: int, ldw: int, x: int, y: int, ldx: int, ldy: int,
+                                stream: int = 0) -> None:
+    _check(load_library().lora_apply_fused_projection(pool, seg, W, ldw, x, y, ldx, ldy, stream),
+           "lora_apply_fused_projection")
+
+
+def lora_fused_projection_stage(pool: int, seg: int, W: int, ldw: int, x: int, y: int, ldx: int, ldy: int,
+                                stage: int, stream: int = 0) -> None:
+    _check(load_library().lora_fused_projection_stage(pool, seg, W, ldw, x, y, ldx, ldy, stage, stream),
+           "lora_fused_projection_stage")
+
+
 # ------------------------------------------------------------ torch helpers
 
 def _stream(stream) -> int:
@@ -335,3 +349,19 @@ def apply_stage(pool: LoraPool, seg: LoraSegments, x, y, stage: int, stream=None
     """One kernel of apply(): 1 = decode path (fused shrink -> expand), 2 = tensor shrink, 3 = tensor expand."""
     lora_apply_stage(pool.handle, seg.handle, x.data_ptr(), y.data_ptr(), x.stride(0), y.stride(0), stage,
                      _stream(stream))
+
+
+def fused_projection(pool: LoraPool, seg: LoraSegments, W, x, y, stream=None) -> None:
+    """y = x @ W^T + delta for every row of the last build (y written, not read).
+    W: bf16 [D, d_in], x: bf16 [T, d_in], y: fp32 [T, D] (row-major views)."""
+    assert W.is_cuda and x.is_cuda and y.is_cuda
+    assert W.element_size() == 2 and x.element_size() == 2 and y.element_size() == 4
+    assert W.stride(1) == 1 and x.stride(1) == 1 and y.stride(1) == 1
+    lora_apply_fused_projection(pool.handle, seg.handle, W.data_ptr(), W.stride(0), x.data_ptr(), y.data_ptr(),
+                                x.stride(0), y.stride(0), _stream(stream))
+
+
+def fused_projection_stage(pool: LoraPool, seg: LoraSegments, W, x, y, stage: int, stream=None) -> None:
+    """One kernel of fused_projection(): 1 = decode shrink, 2 = tensor shrink (both in row mode), 3 = the GEMM."""
+    lora_fused_projection_stage(pool.handle, seg.handle, W.data_ptr(), W.stride(0), x.data_ptr(), y.data_ptr(),
+                                x.stride(0), y.stride(0), stage, _stream(stream))

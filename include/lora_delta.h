@@ -269,6 +269,42 @@ int lora_apply_stage(const lora_pool* pool, const lora_segments* seg, const void
 int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lora_segments* seg, const void* x,
                                      float* y, int64_t ldx, int64_t ldy, lora_stream_t stream);
 
+/* ------------------------------------------------------ fused projection --
+ * The projection with the delta in its own accumulator: for every row t of
+ * the last build on `seg` (slot 0 rows included),
+ *     y[t][c] = sum_j x[t][j] * W[c][j] + delta[t][c]
+ * written once (y is not read).  The delta is added to the projection's fp32
+ * partial sum (TensorFold PR #47, the paragraph on the delta), so it needs no
+ * pass of its own over y (xLLM PR #2014, New subsystems, the
+ * LoRARowParallelLinear item's fused mode, where the base's own output
+ * carries the delta partial sum).  delta is 0 for slot-0 rows and rank-0 lanes.
+ *   W: device bf16 [D][ldw], D = sum of lane_d_out (the lanes' weights
+ *      stacked in lane order, as a linear layer stores [out][in]);
+ *      ldw >= d_in, ldw % 8 == 0, 16-byte aligned.
+ *   x, y, ldx, ldy: as for lora_apply_shrink_expand (y is written, not updated).
+ * Arithmetic: one tcgen05 GEMM over tiles of 128 rows x 256 columns, bf16
+ * products summed in fp32 over d_in in a fixed order; the expand of every slot
+ * present in a tile goes into the same fp32 accumulator as MMAs whose
+ * rank-space input is u' = scale * (A @ x) split into bf16 hi and lo halves
+ * (u' from the two shrinks, run before it in a row mode that writes u' to the
+ * pool's per-row scratch; rows of other slots take zeros).  A row's bits
+ * depend only on its own x row, W and its own adapter.
+ * Kernels: the decode shrink (side stream, as in lora_apply_shrink_expand) and
+ * the tensor shrink when the pool has a loaded lane, then the GEMM.  If the
+ * build found a routing error (or a kernel timed out), the GEMM writes nothing.
+ * T = 0 launches nothing.  Errors: LORA_ERR_ARG, LORA_ERR_SHAPE,
+ * LORA_ERR_CUDA; device timeouts set LORA_ERR_TIMEOUT in the status word. */
+int lora_apply_fused_projection(const lora_pool* pool, const lora_segments* seg, const void* W,
+                                int64_t ldw, const void* x, float* y, int64_t ldx, int64_t ldy,
+                                lora_stream_t stream);
+
+/* One kernel of lora_apply_fused_projection, for per-kernel timing: stage 1 =
+ * decode shrink (row mode), 2 = tensor shrink (row mode), 3 = the GEMM.
+ * Running stages 1..3 in order on one stream gives exactly its result. */
+int lora_fused_projection_stage(const lora_pool* pool, const lora_segments* seg, const void* W,
+                                int64_t ldw, const void* x, float* y, int64_t ldx, int64_t ldy,
+                                int stage, lora_stream_t stream);
+
 /* ----------------------------------------------------------------- misc -- */
 
 /* Text of a status code. */

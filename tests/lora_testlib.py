@@ -99,3 +99,29 @@ def assert_rows_untouched(y_gpu: np.ndarray, y0: np.ndarray, rows):
         a = np.ascontiguousarray(y_gpu[rows]).view(np.uint32)
         b = np.ascontiguousarray(y0[rows]).view(np.uint32)
         assert np.array_equal(a, b), "rows that must not be written were changed"
+
+
+def remix_batch(wl, rng):
+    """A new batch around some of wl's sequences: about half of them, in a new
+    order, with foreign sequences (other slots, lengths on both sides of the
+    tensor-path threshold and of the tile size, base rows) between them.
+    Returns (ids, lens, pieces) where pieces[i] is the source sequence of new
+    sequence i, or None for a foreign one."""
+    S, N = wl.S, wl.num_slots
+    keep = rng.permutation(S)[:max(1, (S + 1) // 2)].tolist()
+    n_foreign = max(3, S // 4)
+    f_lens = rng.choice([1, 1, 1, 2, 5, 63, 64, 65, 127, 130, 300], size=n_foreign).tolist()
+    f_ids = rng.integers(0, N, size=n_foreign).tolist()
+    order = [("k", s) for s in keep] + [("f", i) for i in range(n_foreign)]
+    order = [order[i] for i in rng.permutation(len(order))]
+    ids, lens, pieces = [], [], []
+    for kind, v in order:
+        if kind == "k":
+            ids.append(int(wl.adapter_ids[v]))
+            lens.append(int(wl.q_seq_lens[v]))
+            pieces.append(v)
+        else:
+            ids.append(int(f_ids[v]))
+            lens.append(int(f_lens[v]))
+            pieces.append(None)
+    return np.array(ids, dtype=np.int32), np.array(lens, dtype=np.int32), pieces

@@ -288,32 +288,6 @@ def test_large_configs_full(oracle_mod, name):
         _oracle_check(oracle_mod, wl, proj, what=f"{name} {proj.name}")
 
 
-def _remix(wl, rng):
-    """A new batch around some of wl's sequences: about half of them, in a new
-    order, with foreign sequences (other slots, lengths on both sides of the
-    tensor-path threshold and of the tile size, base rows) between them.
-    Returns (ids, lens, pieces) where pieces[i] is the source sequence of new
-    sequence i, or None for a foreign one."""
-    S, N = wl.S, wl.num_slots
-    keep = rng.permutation(S)[:max(1, (S + 1) // 2)].tolist()
-    n_foreign = max(3, S // 4)
-    f_lens = rng.choice([1, 1, 1, 2, 5, 63, 64, 65, 127, 130, 300], size=n_foreign).tolist()
-    f_ids = rng.integers(0, N, size=n_foreign).tolist()
-    order = [("k", s) for s in keep] + [("f", i) for i in range(n_foreign)]
-    order = [order[i] for i in rng.permutation(len(order))]
-    ids, lens, pieces = [], [], []
-    for kind, v in order:
-        if kind == "k":
-            ids.append(int(wl.adapter_ids[v]))
-            lens.append(int(wl.q_seq_lens[v]))
-            pieces.append(v)
-        else:
-            ids.append(int(f_ids[v]))
-            lens.append(int(f_lens[v]))
-            pieces.append(None)
-    return np.array(ids, dtype=np.int32), np.array(lens, dtype=np.int32), pieces
-
-
 @pytest.mark.parametrize("name", W.CONFIG_NAMES)
 def test_config_batch_mix_invariance(name):
     # At each configuration's own shape: the kept sequences' rows keep their
@@ -322,7 +296,7 @@ def test_config_batch_mix_invariance(name):
     # every adapter sits under another slot label.
     wl = W.make_workload(name)
     rng = np.random.default_rng(sum(map(ord, name)))
-    ids, lens, pieces = _remix(wl, rng)
+    ids, lens, pieces = TL.remix_batch(wl, rng)
     N = wl.num_slots
     n2 = min(2 * N, 2048)
     labels = rng.permutation(np.arange(1, n2))[:N - 1]

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kFpThreads, 1)
                       const __grid_constant__ TmapSized tm_bk, FpParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kFpStages], empty_bar[kFpStages], ufull_bar[kFpStages];
-  __shared__ __align__(8) uint64_t plan_bar, done_bar;
+  __shared__ __align__(8) uint64_t plan_bar, main_bar, done_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int fail_sh, nslots_sh;
   __shared__ uint32_t bits_sh[kFpSlotWords];
@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kFpThreads, 1)
       mbar_init(&ufull_bar[s], 4);
     }
     mbar_init(&plan_bar, 1);
+    mbar_init(&main_bar, 1);
     mbar_init(&done_bar, 1);
     fail_sh = 0;
     nslots_sh = 0;
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kFpThreads, 1)
                    idesc_main, (kb | kk) != 0 ? 1u : 0u);
         mma_commit(&empty_bar[s]);
       }
+      if (ok) mma_commit(&main_bar);  // every stage's K-loop uses are done once this arrives
       if (ok && !mbar_wait_or_fail(&plan_bar, 0, &fail_sh)) {
         fail_sh = 1;
         ok = false;
@@ -280,10 +282,22 @@ __global__ void __launch_bounds__(kFpThreads, 1)
     // u' operands of the expand steps: row m of the slot's rows, zero for
     // rows of other slots, as bf16 hi and lo in the K-major core-matrix
     // layout (8 rows x 16 bytes per core matrix; 16 ranks = two of them)
+    // A parity wait names one of two phases, so it is only sound while the
+    // barrier is at most one phase behind the awaited one.  These warps skip
+    // the K loop's stage uses; they start once its MMAs are complete, and from
+    // then on wait for every expand use of a stage in order.
     bool ok = true;
+    {
+      int got = 1;
+      if (nslots_sh > 0 && lane == 0) got = mbar_wait_or_fail(&main_bar, 0, &fail_sh) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, got, 0)) {
+        fail_sh = 1;
+        ok = false;
+      }
+    }
     uint32_t i = (uint32_t)p.nkb;
     const uint32_t row_off = (uint32_t)((m >> 3) * 256 + (m & 7) * 16);
-    for_each_step(p, slots_sh, nslots_sh, n0, [&](int k, int l, int q0, int ng, int, int, int) {
+    if (ok) for_each_step(p, slots_sh, nslots_sh, n0, [&](int k, int l, int q0, int ng, int, int, int) {
       const int s = (int)(i % kFpStages);
       if (i >= kFpStages) {  // one lane waits for the stage to be free; the warp follows it
         int got = 1;

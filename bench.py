@@ -502,6 +502,140 @@ def time_e2e(wl, ctx, steps, warmup, dev):
     return ms, h2d, d2h
 
 
+def fused_units(wl):
+    """Algorithmic flops and bytes of the fused projection (y = x W^T + delta)
+    per projection: 2 T D d_in flops of the base product plus the delta's;
+    bytes = x and W read once, y written once (4 B per element), the present
+    factors once."""
+    out = []
+    slot = np.repeat(wl.adapter_ids, wl.q_seq_lens)
+    for proj in wl.projections:
+        T, D, K = wl.T, proj.D, proj.d_in
+        flops = 2 * T * D * K
+        byts = 2 * T * K + 2 * D * K + 4 * T * D
+        for k in np.unique(slot[slot != 0]):
+            n = int((slot == k).sum())
+            for l in range(proj.num_lanes):
+                r = int(proj.rank[k, l])
+                if r > 0:
+                    flops += n * 2 * r * (K + proj.lane_d_out[l])
+                    byts += 2 * r * (K + proj.lane_d_out[l])
+        out.append({"flops": int(flops), "bytes": int(byts)})
+    return out
+
+
+def _library_mm(xb, wb, y):
+    """y = x W^T by the library GEMM (cuBLAS through torch), fp32 output when
+    torch offers it; returns a label of what ran."""
+    import torch
+    try:
+        torch.mm(xb, wb.t(), out_dtype=torch.float32, out=y)
+        return "torch.mm bf16 x bf16 -> fp32 (cuBLAS)"
+    except (TypeError, RuntimeError):
+        y.copy_(torch.mm(xb, wb.t()))
+        return "torch.mm bf16 x bf16 -> bf16 (cuBLAS), copied to fp32 y"
+
+
+def time_fused(wl, steps, warmup, dev):
+    """The fused projection of every projection of a workload (graph replays
+    with L2 flushed between them): the whole step (build + fused projections),
+    the GEMM kernel alone, and, for comparison, the library GEMM (cuBLAS) with
+    the separate delta apply after it."""
+    import torch
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    projs, seg, ids, lens = setup_device_workload(wl, dev)
+    for i, pr in enumerate(projs):
+        pr["W"] = torch.from_numpy(W.projection_weight(pr["proj"], seed=1 + i).view(np.int16)).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    T = wl.T
+
+    def build():
+        LD.lora_build_segments(seg.handle, ids.data_ptr(), lens.data_ptr(), wl.S, T, stream.cuda_stream)
+
+    def fused_step():
+        build()
+        for pr in projs:
+            LD.fused_projection(pr["pool"], seg, pr["W"], pr["x"], pr["y"])
+
+    def gemm_only():
+        for pr in projs:
+            LD.fused_projection_stage(pr["pool"], seg, pr["W"], pr["x"], pr["y"], 3)
+
+    label = [None]
+
+    def library_step():
+        build()
+        for pr in projs:
+            label[0] = _library_mm(pr["x"].view(torch.bfloat16), pr["W"].view(torch.bfloat16), pr["y"])
+            LD.apply(pr["pool"], seg, pr["x"], pr["y"])
+
+    def library_gemm():
+        for pr in projs:
+            _library_mm(pr["x"].view(torch.bfloat16), pr["W"].view(torch.bfloat16), pr["y"])
+
+    # eager reference bits of the fused step
+    fused_step()
+    torch.cuda.synchronize()
+    assert seg.status() == 0, LD.lora_status_string(seg.status())
+    y_eager = [pr["y"].clone() for pr in projs]
+    library_step()  # warms cuBLAS outside any capture
+    torch.cuda.synchronize()
+
+    def graph_ms(fn, check=False):
+        g = torch.cuda.CUDAGraph()
+        n0 = LD.lora_launch_count()
+        with torch.cuda.graph(g):
+            fn()
+        launches = LD.lora_launch_count() - n0
+        if check:
+            g.replay()
+            torch.cuda.synchronize()
+            for pr, ye in zip(projs, y_eager):
+                assert torch.equal(pr["y"].view(torch.int32), ye.view(torch.int32)), "fused replay differs"
+        for _ in range(warmup):
+            flush.fill_(1)
+            g.replay()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs), launches
+
+    f_ms, f_launch = graph_ms(fused_step, check=True)
+    fused_step()  # u' of this step in the pools for the GEMM-only replays
+    g_ms, _ = graph_ms(gemm_only)
+    l_ms, _ = graph_ms(library_step)
+    lg_ms, _ = graph_ms(library_gemm)
+    assert seg.status() == 0, LD.lora_status_string(seg.status())
+    del flush, projs
+    torch.cuda.empty_cache()
+    return {"step_ms": f_ms, "gemm_ms": g_ms, "library_step_ms": l_ms, "library_gemm_ms": lg_ms,
+            "launches_per_step": f_launch, "library": label[0]}
+
+
+def fused_record(wl, fr, bf16_peak, hbm_peak):
+    units = fused_units(wl)
+    flops = sum(u["flops"] for u in units)
+    byts = sum(u["bytes"] for u in units)
+    g = fr["gemm_ms"] * 1e-3
+    return {"step_ms": round(fr["step_ms"], 5), "gemm_ms": round(fr["gemm_ms"], 5),
+            "tokens_per_s": round(wl.T / (fr["step_ms"] * 1e-3), 1),
+            "alg_flops": int(flops), "alg_bytes": int(byts),
+            "gemm_tflops": round(flops / g / 1e12, 2), "gemm_frac_bf16": round(flops / g / 1e12 / bf16_peak, 4),
+            "gemm_gbs": round(byts / g / 1e9, 1), "gemm_frac_hbm": round(byts / g / 1e9 / hbm_peak, 4),
+            "library_step_ms": round(fr["library_step_ms"], 5), "library_gemm_ms": round(fr["library_gemm_ms"], 5),
+            "library": fr["library"],
+            "speedup_vs_library_step": round(fr["library_step_ms"] / fr["step_ms"], 3),
+            "launches_per_step": fr["launches_per_step"],
+            "note": "y = x W^T + delta with the delta in the GEMM's accumulator (one y write); library_step = "
+                    "the library GEMM then the separate delta apply (y written, read and written again)"}
+
+
 def cpu_oracle_rates(wl, threads: int, target_s: float, runs: int = 3, seed: int = 0):
     """The oracle (as it is) on `threads` host threads (0 = all cores).
 
@@ -697,7 +831,10 @@ def per_workload_summary(args, dev, hbm_peak, bf16_peak, headline):
     import torch
     out = {}
     h_name, h_res, with_cpu = headline
+    only = [n for n in args.only.split(",") if n]
     for name in W.CONFIG_NAMES:
+        if only and name not in only:
+            continue
         wl = W.make_workload(name, seed=args.seed)
         if name == h_name and not args.max_seqs:
             res = h_res
@@ -707,11 +844,16 @@ def per_workload_summary(args, dev, hbm_peak, bf16_peak, headline):
             torch.cuda.empty_cache()
         rec = workload_record(wl, res, hbm_peak, bf16_peak)
         rec["clocks"] = res["clocks"]
+        if not args.no_fused:
+            rec["fused_projection"] = fused_record(wl, time_fused(wl, args.steps, args.warmup, dev), bf16_peak,
+                                                   hbm_peak)
         if with_cpu:
             rec["cpu_oracle"] = {"threads_1": cpu_oracle_rates(wl, 1, args.cpu_seconds_detail),
                                  "threads_all": cpu_oracle_rates(wl, 0, args.cpu_seconds_detail)}
         out[name] = rec
     for name in W.MOE_CONFIG_NAMES:
+        if only and name not in only:
+            continue
         # MoE expert LoRA (not one of the five reference configurations)
         wl = W.make_moe_workload(name, seed=args.seed)
         res, ctx = time_ours(wl, args.steps, args.warmup, dev, 0)
@@ -786,6 +928,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--headline-only", action="store_true", help="skip the per_workload records of all configs")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused-projection records")
+    ap.add_argument("--only", default="", help="per_workload: only these comma-separated configurations")
     ap.add_argument("--max-seqs", type=int, default=0,
                     help="keep only the first N sequences of the workload (smaller case for profiler captures)")
     args = ap.parse_args()

@@ -103,6 +103,8 @@ struct lora_segments {
   int4* tc_work = nullptr;
   int32_t* run_ids = nullptr;   // [max_seqs] per-run slots of a dispatched-row (MoE) build
   int32_t* run_lens = nullptr;  // [max_seqs] per-run lengths; the run count is counts[8]
+  int32_t* seq_scratch = nullptr;  // [6][max_seqs] the builder's per-sequence arrays when they do not
+                                   // fit in its shared memory (else unused)
 };
 
 namespace lora {

@@ -43,6 +43,8 @@ struct SegParams {
   int4* dec_work;
   int32_t* dec_rows;
   int4* tc_work;
+  int32_t* seq_scratch;  // [6][S] per-sequence arrays when they do not fit in shared memory
+  int seq_smem;          // 1: the per-sequence arrays are in shared memory
 };
 
 // Exclusive prefix sum over the block (all threads call it).  `sums` is a
@@ -156,104 +158,92 @@ __device__ __forceinline__ void warp_fill(int32_t* dst, int n, int v0, int step,
   for (int j = head + 4 * n4 + lane; j < n; j += 32) dst[j] = v0 + j * step;
 }
 
-// Shared memory of the builder, in ints: six per-sequence arrays of S and
-// the per-key tables (2N + 2N + N + (N + 1) + (N + 1)).
-size_t seg_smem_ints(int N, int S) { return 6 * (size_t)S + 7 * (size_t)N + 2; }
+// Shared memory of the builder, in ints: the per-key tables
+// (2N + 2N + N + (N + 1) + (N + 1)), then, when they fit, six per-sequence
+// arrays of S (else those live in the workspace's sequence scratch).
+size_t seg_key_ints(int N) { return 7 * (size_t)N + 2; }
+bool seq_arrays_in_smem(int N, int S) { return sizeof(int) * (seg_key_ints(N) + 6 * (size_t)S) <= kSegSmemLimit; }
 
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) {
   extern __shared__ int smem_dyn[];
   __shared__ int scan_sums[3][33];
-  __shared__ long long warp_len[kSegThreads / 32];
-  __shared__ int warp_bad[kSegThreads / 32];
+  __shared__ int bad_sh;
+  __shared__ unsigned long long len_sh;
   pdl_launch_next();  // the apply kernels may be scheduled now; they wait for this grid
   pdl_wait();         // the previous kernel's results are visible from here on
 
   const int N = p.N, Scap = p.S, T = p.T;
-  int* s_len = smem_dyn;              // [S] q_len
-  int* s_id = s_len + Scap;           // [S] slot
-  int* s_start = s_id + Scap;         // [S] first row
-  int* s_pos = s_start + Scap;        // [S] rank of the first row inside its (class, slot) bin
-  int* s_tile = s_pos + Scap;         // [S] rank of the first tile inside its slot's tiles
-  int* s_key = s_tile + Scap;         // [S] (class, slot) key, -1 if the sequence is inactive; bits 24..28:
-                                   //     the last lane of its warp with the same key
-  int* cnt_tok = s_key + Scap;     // [2N] rows per (class, slot), then their first perm position
+  int* cnt_tok = smem_dyn;         // [2N] rows per (class, slot), then their first perm position
   int* run_tok = cnt_tok + 2 * N;  // [2N] running position while ranking sequences
   int* cnt_tile = run_tok + 2 * N; // [N]  class-1 tiles per slot, then the first tile index
   int* dec_cnt = cnt_tile + N;     // [N+1] decode groups per slot, then the first group index
   int* tc_cnt = dec_cnt + N + 1;   // [N+1] class-1 tiles per slot (scan input), then the first tile
+  int* seqa = p.seq_smem ? tc_cnt + N + 1 : p.seq_scratch;
+  int* s_len = seqa;                // [S] q_len
+  int* s_id = s_len + Scap;         // [S] slot
+  int* s_start = s_id + Scap;       // [S] first row
+  int* s_pos = s_start + Scap;      // [S] rank of the first row inside its (class, slot) bin
+  int* s_tile = s_pos + Scap;       // [S] rank of the first tile inside its slot's tiles
+  int* s_key = s_tile + Scap;       // [S] (class, slot) key, -1 if the sequence is inactive; bits 24..28:
+                                    //     the last lane of its warp with the same key
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kLeadShift = 24, kKeyMask = (1 << kLeadShift) - 1;  // keys < 2N <= 4096
   // the sequence count (from the device when a run-length pass wrote it)
   const int S = p.S_dev ? min(max(*p.S_dev, 0), Scap) : Scap;
 
-  // ---- load the sequences once; validation by block reductions
   for (int i = tid; i < 2 * N; i += kSegThreads) run_tok[i] = 0;
   for (int i = tid; i < N; i += kSegThreads) cnt_tile[i] = 0;
-  long long my_sum = 0;
-  int my_bad = 0;  // bit 0: a negative length, bit 1: an id out of range
-  for (int s = tid; s < S; s += kSegThreads) {
-    const int len = p.lens[s], id = p.ids[s];
-    s_len[s] = len;
-    s_id[s] = id;
-    my_bad |= (len < 0 ? 1 : 0) | ((id < 0 || id >= N) ? 2 : 0);
-    my_sum += len;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    my_sum += __shfl_xor_sync(0xffffffffu, my_sum, o);
-    my_bad |= __shfl_xor_sync(0xffffffffu, my_bad, o);
-  }
-  if (lane == 0) {
-    warp_len[warp] = my_sum;
-    warp_bad[warp] = my_bad;
-  }
-  __syncthreads();
-  long long total_len = lane < kSegThreads / 32 ? warp_len[lane] : 0;
-  int bad = lane < kSegThreads / 32 ? warp_bad[lane] : 0;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    total_len += __shfl_xor_sync(0xffffffffu, total_len, o);
-    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-  }
-  if ((bad & 1) || total_len != (long long)T || (bad & 2)) {
-    if (tid < 4) p.counts[tid] = 0;
-    if (tid == 0) *p.status = ((bad & 1) || total_len != (long long)T) ? LORA_ERR_META : LORA_ERR_SLOT;
-    return;
+  if (tid == 0) {
+    bad_sh = 0;
+    len_sh = 0ull;
   }
 
-  // ---- per sequence: first row (block scan), key, and its rank among the
-  // earlier lanes of its warp with the same key (rows and tiles)
-  int carry = 0;
+  // ---- per sequence, 512 at a time: length, slot, key, first row (block
+  // scan), and its rank among the earlier lanes of its warp with the same
+  // key (rows and tiles; lanes of one key found with one match)
+  int carry = 0, bad = 0;  // bad bit 0: a negative length, bit 1: an id out of range
+  long long my_len = 0;
   for (int b = 0; b < S; b += kSegThreads) {
     const int s = b + tid;
     int key = -1, len = 0, nt = 0;
     if (s < S) {
-      len = s_len[s];
-      const int id = s_id[s];
-      if (id != 0 && len > 0) {
+      len = p.lens[s];
+      const int id = p.ids[s];
+      bad |= (len < 0 ? 1 : 0) | ((id < 0 || id >= N) ? 2 : 0);
+      my_len += len;
+      s_len[s] = len;
+      s_id[s] = id;
+      if (id > 0 && id < N && len > 0) {
         const int cls = len >= LORA_TC_MIN_QLEN ? 1 : 0;
         key = cls * N + id;
         nt = cls ? (len + kTcTile - 1) / kTcTile : 0;
       }
     }
-    int tot;
-    const int ex = block_exclusive_scan(s < S ? len : 0, scan_sums[0], tot);
-    int pl = 0, pt = 0, lead = lane;
-#pragma unroll 4
-    for (int j = 0; j < 32; ++j) {
-      const int kj = __shfl_sync(0xffffffffu, key, j);
-      const int lj = __shfl_sync(0xffffffffu, len, j);
-      const int tj = __shfl_sync(0xffffffffu, nt, j);
-      if (kj == key) {
-        if (j < lane) {
+    const unsigned m = __match_any_sync(0xffffffffu, key);
+    const unsigned below = m & ((1u << lane) - 1u);
+    const int lead = 31 - __clz(m);
+    int pl, pt;
+    // when every lane of a key has the same length the rank is a count
+    const unsigned m_len = __match_any_sync(0xffffffffu, ((unsigned long long)(unsigned)key << 32) | (unsigned)len);
+    if (__all_sync(0xffffffffu, m_len == m)) {
+      pl = __popc(below) * len;
+      pt = __popc(below) * nt;
+    } else {
+      pl = pt = 0;
+      unsigned rem = below;
+      while (__any_sync(0xffffffffu, rem != 0)) {
+        const int j = rem ? __ffs(rem) - 1 : lane;
+        const int lj = __shfl_sync(0xffffffffu, len, j), tj = __shfl_sync(0xffffffffu, nt, j);
+        if (rem) {
           pl += lj;
           pt += tj;
-        } else if (j > lane) {
-          lead = j;
+          rem &= rem - 1u;
         }
       }
     }
+    int tot;
+    const int ex = block_exclusive_scan(s < S ? len : 0, scan_sums[0], tot);
     if (s < S) {
       s_start[s] = carry + ex;
       p.seq_start[s] = carry + ex;
@@ -263,17 +253,43 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
     }
     carry += tot;
   }
-  if (tid == 0) p.seq_start[S] = T;
+  // validation: order-free reductions
+  if (bad) atomicOr(&bad_sh, bad);
+  if (my_len) atomicAdd(&len_sh, (unsigned long long)my_len);
   __syncthreads();
+  {
+    const int bb = bad_sh;
+    if ((bb & 1) || len_sh != (unsigned long long)(long long)T || (bb & 2)) {
+      if (tid < 4) p.counts[tid] = 0;
+      if (tid == 0) *p.status = ((bb & 1) || len_sh != (unsigned long long)(long long)T) ? LORA_ERR_META
+                                                                                        : LORA_ERR_SLOT;
+      return;
+    }
+  }
+  if (tid == 0) p.seq_start[S] = T;
 
   // ---- stable ranks: one warp walks the sequences 32 at a time in index
-  // order; the per-key running counts end as the rows per (class, slot) and
-  // the tiles per slot
+  // order (the next chunk's entries are read ahead); the per-key running
+  // counts end as the rows per (class, slot) and the tiles per slot
   if (warp == 0) {
+    auto fetch = [&](int s, int& kk, int& pl, int& pt, int& len) {
+      if (s < S) {
+        kk = s_key[s];
+        pl = s_pos[s];
+        pt = s_tile[s];
+        len = s_len[s];
+      } else {
+        kk = -1;
+        pl = pt = len = 0;
+      }
+    };
+    int kk, pl, pt, len;
+    fetch(lane, kk, pl, pt, len);
     for (int b = 0; b < S; b += 32) {
-      const int s = b + lane, sc = min(s, S - 1);
-      const int kk = s_key[sc], pl = s_pos[sc], pt = s_tile[sc], len = s_len[sc];
-      const bool act = s < S && kk >= 0;
+      int kk2, pl2, pt2, len2;
+      fetch(b + 32 + lane, kk2, pl2, pt2, len2);
+      const int s = b + lane;
+      const bool act = kk >= 0;
       const int key = act ? (kk & kKeyMask) : 0;
       const int lead = act ? (kk >> kLeadShift) : lane;
       const bool tc = key >= N, last = act && lead == lane;
@@ -296,6 +312,10 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
         if (tc) cnt_tile[id] = base_tile + pt + (len + kTcTile - 1) / kTcTile;
       }
       __syncwarp();  // this chunk's counts are visible to the next chunk's reads
+      kk = kk2;
+      pl = pl2;
+      pt = pt2;
+      len = len2;
     }
   }
   __syncthreads();
@@ -323,7 +343,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
 
   // ---- per-token slot and perm, and the tensor tiles.  A thread writes the
   // rows of each short sequence it owns (decode rows); the longer ones are
-  // dealt out to the warps in index order, one warp to a sequence.
+  // dealt out to the warps in index order (the k-th long sequence to warp
+  // k mod warps), one warp to a sequence.
   for (int s = tid; s < S; s += kSegThreads) {
     const int kk = s_key[s], len = s_len[s], id = s_id[s], st = s_start[s];
     if (len <= kShortSeq) {
@@ -343,23 +364,21 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
         p.tc_work[base + i] = make_int4(id, rb, min(rb + kTcTile, st + len), s);
     }
   }
-  // the long sequences, compacted into a list (in s_tile, which is no longer
-  // read once the tiles above are written), then one warp to each
-  int my_long = 0;
-  for (int s = tid; s < S; s += kSegThreads) my_long += s_len[s] > kShortSeq ? 1 : 0;
-  int n_long;
-  int li = block_exclusive_scan(my_long, scan_sums[0], n_long);  // barriers: the tiles are written
-  int* long_list = s_tile;
-  for (int s = tid; s < S; s += kSegThreads)
-    if (s_len[s] > kShortSeq) long_list[li++] = s;
-  __syncthreads();
-  for (int i = warp; i < n_long; i += kSegThreads / 32) {
-    const int s = long_list[i];
-    const int id = s_id[s], st = s_start[s], len = s_len[s], kk = s_key[s];
-    warp_fill(p.slot + st, len, id, 0, lane);
-    if (kk >= 0) warp_fill(p.perm + cnt_tok[kk & kKeyMask] + s_pos[s], len, st, 1, lane);
-    if (kk >= 0 && (kk & kKeyMask) < N)  // decode rows (a sequence shorter than the tensor threshold)
-      warp_fill(p.dec_rows + dec_cnt[kk & kKeyMask] * kDecGroup + s_pos[s], len, st, 1, lane);
+  {
+    int n_long = 0;  // long sequences before this chunk
+    for (int b = 0; b < S; b += 32) {
+      const int s = b + lane;
+      const unsigned lm = __ballot_sync(0xffffffffu, s < S && s_len[s] > kShortSeq);
+      for (unsigned r = lm; r; r &= r - 1u, ++n_long) {
+        if (n_long % (kSegThreads / 32) != warp) continue;
+        const int sq = b + __ffs(r) - 1;
+        const int id = s_id[sq], st = s_start[sq], len = s_len[sq], kk = s_key[sq];
+        warp_fill(p.slot + st, len, id, 0, lane);
+        if (kk >= 0) warp_fill(p.perm + cnt_tok[kk & kKeyMask] + s_pos[sq], len, st, 1, lane);
+        if (kk >= 0 && (kk & kKeyMask) < N)  // decode rows (a sequence shorter than the tensor threshold)
+          warp_fill(p.dec_rows + dec_cnt[kk & kKeyMask] * kDecGroup + s_pos[sq], len, st, 1, lane);
+      }
+    }
   }
 
   // ---- decode groups: slot k's class-0 run cut into runs of <= kDecGroup
@@ -479,7 +498,9 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
   p.dec_work = seg->dec_work;
   p.dec_rows = seg->dec_rows;
   p.tc_work = seg->tc_work;
-  const size_t sm = sizeof(int) * seg_smem_ints(seg->N, S);
+  p.seq_scratch = seg->seq_scratch;
+  p.seq_smem = seq_arrays_in_smem(seg->N, S) ? 1 : 0;
+  const size_t sm = sizeof(int) * (seg_key_ints(seg->N) + (p.seq_smem ? 6 * (size_t)S : 0));
   if (sm > 48 * 1024 && !set_smem_limit(reinterpret_cast<const void*>(seg_build_kernel), seg->device, (int)sm))
     return LORA_ERR_CUDA;
   const cudaError_t e = launch_pdl(seg_build_kernel, dim3(1), dim3(kSegThreads), sm, st, p);
@@ -494,7 +515,8 @@ using namespace lora;
 namespace {
 
 struct SegLayout {
-  size_t status, counts, seq_start, slot, perm, seg_off, dec_work, dec_rows, tc_work, run_ids, run_lens, total;
+  size_t status, counts, seq_start, slot, perm, seg_off, dec_work, dec_rows, tc_work, run_ids, run_lens, seq_scratch,
+      total;
   int cap_dec, cap_tc;
 };
 
@@ -502,8 +524,8 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 bool seg_layout(int max_seqs, int max_tokens, int N, SegLayout* L) {
   if (max_seqs < 1 || max_tokens < 1 || N < 2 || N > LORA_MAX_SLOTS) return false;
-  // the builder keeps every sequence and every slot's counters in shared memory
-  if (sizeof(int) * seg_smem_ints(N, max_seqs) > kSegSmemLimit) return false;
+  // the builder keeps every slot's counters in shared memory
+  if (sizeof(int) * seg_key_ints(N) > kSegSmemLimit) return false;
   L->cap_dec = ceil_div(max_tokens, kDecGroup) + N;
   L->cap_tc = ceil_div(max_tokens, kTcTile) + max_seqs;
   size_t o = 0;
@@ -518,6 +540,9 @@ bool seg_layout(int max_seqs, int max_tokens, int N, SegLayout* L) {
   L->tc_work = o; o = align256(o + 16 * (size_t)L->cap_tc);
   L->run_ids = o; o = align256(o + 4 * (size_t)max_seqs);
   L->run_lens = o; o = align256(o + 4 * (size_t)max_seqs);
+  // per-sequence arrays of the builder for steps whose sequences do not fit in shared memory
+  L->seq_scratch = o;
+  if (!seq_arrays_in_smem(N, max_seqs)) o = align256(o + 4 * 6 * (size_t)max_seqs);
   L->total = o;
   return true;
 }
@@ -561,6 +586,7 @@ int lora_segments_create(lora_segments** out, void* dev_ws, size_t ws_bytes, int
   s->tc_work = reinterpret_cast<int4*>(b + L.tc_work);
   s->run_ids = reinterpret_cast<int32_t*>(b + L.run_ids);
   s->run_lens = reinterpret_cast<int32_t*>(b + L.run_lens);
+  s->seq_scratch = reinterpret_cast<int32_t*>(b + L.seq_scratch);
   *out = s;
   return LORA_OK;
 }

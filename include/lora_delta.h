@@ -140,9 +140,10 @@ int lora_pool_destroy(lora_pool* pool);
  */
 
 /* Bytes of device workspace for up to max_seqs sequences, max_tokens rows and num_slots slots
- * (0 if the shape is invalid).  The builder keeps every sequence and every slot's counters in
- * one CTA's shared memory, so 4 * (6 * max_seqs + 7 * num_slots + 2) must not exceed
- * 227 KiB - 2 KiB (max_seqs <= 7210 at num_slots = 2048, <= 9523 at num_slots = 65). */
+ * (0 if the shape is invalid).  The builder keeps every slot's counters in one CTA's shared
+ * memory, and its six per-sequence arrays there too when 4 * (6 * max_seqs + 7 * num_slots + 2)
+ * fits in 227 KiB - 2 KiB; beyond that the workspace holds them (24 bytes per sequence more),
+ * so max_seqs has no limit of its own. */
 size_t lora_segments_bytes(int max_seqs, int max_tokens, int num_slots);
 
 /* Create a segments descriptor over caller workspace dev_ws (256-byte aligned). */

@@ -65,11 +65,12 @@ def test_segments_bytes(lib):
     assert LD.lora_segments_bytes(0, 16, 4) == 0
     assert LD.lora_segments_bytes(4, 16, 1) == 0
     assert LD.lora_segments_bytes(4, 16, 4097) == 0
-    # the builder holds 6 ints per sequence and 7 per slot (+2) in 227 KiB - 2 KiB of shared memory
-    assert LD.lora_segments_bytes(7210, 16, 2048) > 0
-    assert LD.lora_segments_bytes(7211, 16, 2048) == 0
-    assert LD.lora_segments_bytes(9523, 16, 65) > 0
-    assert LD.lora_segments_bytes(9524, 16, 65) == 0
+    # the builder's per-sequence arrays move to the workspace (24 bytes a sequence) once they no
+    # longer fit next to the per-slot counters in 227 KiB - 2 KiB of shared memory: no cap on max_seqs
+    a, b = LD.lora_segments_bytes(7210, 16, 2048), LD.lora_segments_bytes(7211, 16, 2048)
+    assert a > 0 and b >= a + 24 * 7211 - 256
+    assert LD.lora_segments_bytes(20000, 16, 65) > LD.lora_segments_bytes(9523, 16, 65) + 24 * 20000 - 256
+    assert LD.lora_segments_bytes(100000, 200000, 2048) > 0
 
 
 def test_host_argument_errors_need_no_gpu(lib):

@@ -84,3 +84,21 @@ def test_rebuild_reuses_workspace(oracle_mod):
         assert np.array_equal(got["perm"], exp["perm"])
         assert np.array_equal(got["tc_work"], exp["tc_work"])
         assert np.array_equal(got["dec_work"], exp["dec_work"])
+
+
+@pytest.mark.parametrize("N", [65, 2048])
+def test_many_sequences_beyond_shared_memory(oracle_mod, N):
+    # 20000 sequences: the builder's per-sequence arrays live in the workspace
+    rng = np.random.default_rng(N)
+    S = 20000
+    lens = rng.choice([0, 1, 1, 1, 2, 5, 64, 130], size=S)
+    ids = rng.integers(0, N, size=S)
+    _compare(oracle_mod, ids, lens, N)
+
+
+def test_equal_and_unequal_lengths_inside_a_warp(oracle_mod):
+    # warps whose same-slot sequences all have one length (ranks are counts)
+    # next to warps where they differ (ranks are sums)
+    ids = [1] * 32 + [2, 1] * 16 + [3] * 16 + [1] * 16
+    lens = [1] * 32 + [1, 2] * 16 + [70] * 16 + [3, 1] * 8
+    _compare(oracle_mod, ids, lens, 4)

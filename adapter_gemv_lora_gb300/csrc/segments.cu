@@ -44,7 +44,7 @@ struct SegParams {
   int32_t* dec_rows;
   int4* tc_work;
   int32_t* seq_scratch;  // [6][S] per-sequence arrays when they do not fit in shared memory
-  int seq_smem;          // 1: the per-sequence arrays are in shared memory
+  int tables;            // 1: per-warp rank tables in shared memory
 };
 
 // Exclusive prefix sum over the block (all threads call it).  `sums` is a
@@ -77,19 +77,24 @@ __device__ int block_exclusive_scan(int v, int* sums, int& total) {
   return ex;
 }
 
-// Three exclusive scans at once over arrays of n0, n1, n2 ints in shared
-// memory (in place: each entry becomes the sum of the entries before it).
-// Each thread takes `per` consecutive entries of every array; the totals are
-// returned.  All threads call it; two barriers.
-__device__ void block_scan3(int* a0, int n0, int* a1, int n1, int* a2, int n2, int per, int (*sums)[33],
-                            int& t0, int& t1, int& t2) {
+// The three exclusive scans of the offsets at once, in shared memory: rows
+// per (class, slot) r[n0] -> o0, decode groups per slot ceil(r[k] / group)
+// (k < n1) -> o1, tiles per slot c[n2] -> o2 (each output entry the sum of
+// the entries before it).  Each thread takes `per` consecutive entries; the
+// totals are returned.  All threads call it; two barriers, and a barrier must
+// separate the sources' last writes from the call.
+__device__ void block_scan3(const int* r, int* o0, int n0, int* o1, int n1, const int* c, int* o2, int n2, int per,
+                            int (*sums)[33], int& t0, int& t1, int& t2) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lo = threadIdx.x * per;
+  auto e0 = [&](int i) { return r[i]; };
+  auto e1 = [&](int i) { return (r[i] + kDecGroup - 1) / kDecGroup; };
+  auto e2 = [&](int i) { return c[i]; };
   int v0 = 0, v1 = 0, v2 = 0;
   for (int i = 0; i < per; ++i) {
-    if (lo + i < n0) v0 += a0[lo + i];
-    if (lo + i < n1) v1 += a1[lo + i];
-    if (lo + i < n2) v2 += a2[lo + i];
+    if (lo + i < n0) v0 += e0(lo + i);
+    if (lo + i < n1) v1 += e1(lo + i);
+    if (lo + i < n2) v2 += e2(lo + i);
   }
   int x0 = v0, x1 = v1, x2 = v2;
 #pragma unroll
@@ -124,19 +129,16 @@ __device__ void block_scan3(int* a0, int n0, int* a1, int n1, int* a2, int n2, i
   int c0 = sums[0][warp] + x0 - v0, c1 = sums[1][warp] + x1 - v1, c2 = sums[2][warp] + x2 - v2;
   for (int i = 0; i < per; ++i) {
     if (lo + i < n0) {
-      const int e = a0[lo + i];
-      a0[lo + i] = c0;
-      c0 += e;
+      o0[lo + i] = c0;
+      c0 += e0(lo + i);
     }
     if (lo + i < n1) {
-      const int e = a1[lo + i];
-      a1[lo + i] = c1;
-      c1 += e;
+      o1[lo + i] = c1;
+      c1 += e1(lo + i);
     }
     if (lo + i < n2) {
-      const int e = a2[lo + i];
-      a2[lo + i] = c2;
-      c2 += e;
+      o2[lo + i] = c2;
+      c2 += e2(lo + i);
     }
   }
   t0 = sums[0][32];
@@ -163,7 +165,16 @@ __device__ __forceinline__ void warp_fill(int32_t* dst, int n, int v0, int step,
 // arrays of S (else those live in the workspace's sequence scratch).
 size_t seg_key_ints(int N) { return 7 * (size_t)N + 2; }
 bool seq_arrays_in_smem(int N, int S) { return sizeof(int) * (seg_key_ints(N) + 6 * (size_t)S) <= kSegSmemLimit; }
+// Per-warp rank tables ([warps][2N] rows and [warps][N] tiles of one chunk of
+// sequences), used when they fit after the arrays above: every warp then
+// ranks its sequences against the earlier warps at once instead of one warp
+// walking the chunk.
+constexpr int kSegWarps = kSegThreads / 32;
+size_t seg_table_ints(int N) { return (size_t)kSegWarps * 3 * N; }
 
+// SEQ_SMEM: the per-sequence arrays are in shared memory (the compiler then
+// knows every access to them is a shared one), else in the workspace.
+template <bool SEQ_SMEM>
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) {
   extern __shared__ int smem_dyn[];
   __shared__ int scan_sums[3][33];
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   int* cnt_tile = run_tok + 2 * N; // [N]  class-1 tiles per slot, then the first tile index
   int* dec_cnt = cnt_tile + N;     // [N+1] decode groups per slot, then the first group index
   int* tc_cnt = dec_cnt + N + 1;   // [N+1] class-1 tiles per slot (scan input), then the first tile
-  int* seqa = p.seq_smem ? tc_cnt + N + 1 : p.seq_scratch;
+  int* seqa = SEQ_SMEM ? tc_cnt + N + 1 : p.seq_scratch;
   int* s_len = seqa;                // [S] q_len
   int* s_id = s_len + Scap;         // [S] slot
   int* s_start = s_id + Scap;       // [S] first row
@@ -186,6 +197,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   int* s_tile = s_pos + Scap;       // [S] rank of the first tile inside its slot's tiles
   int* s_key = s_tile + Scap;       // [S] (class, slot) key, -1 if the sequence is inactive; bits 24..28:
                                     //     the last lane of its warp with the same key
+  int* tab_rows = tc_cnt + N + 1 + (SEQ_SMEM ? 6 * Scap : 0);  // [warps][2N] (when p.tables)
+  int* tab_tiles = tab_rows + kSegWarps * 2 * N;               // [warps][N]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kLeadShift = 24, kKeyMask = (1 << kLeadShift) - 1;  // keys < 2N <= 4096
@@ -202,16 +215,15 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   // ---- per sequence, 512 at a time: length, slot, key, first row (block
   // scan), and its rank among the earlier lanes of its warp with the same
   // key (rows and tiles; lanes of one key found with one match)
-  int carry = 0, bad = 0;  // bad bit 0: a negative length, bit 1: an id out of range
-  long long my_len = 0;
+  int carry = 0;
   for (int b = 0; b < S; b += kSegThreads) {
     const int s = b + tid;
     int key = -1, len = 0, nt = 0;
+    int bad = 0;  // bit 0: a negative length, bit 1: an id out of range
     if (s < S) {
       len = p.lens[s];
       const int id = p.ids[s];
-      bad |= (len < 0 ? 1 : 0) | ((id < 0 || id >= N) ? 2 : 0);
-      my_len += len;
+      bad = (len < 0 ? 1 : 0) | ((id < 0 || id >= N) ? 2 : 0);
       s_len[s] = len;
       s_id[s] = id;
       if (id > 0 && id < N && len > 0) {
@@ -244,6 +256,18 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
     }
     int tot;
     const int ex = block_exclusive_scan(s < S ? len : 0, scan_sums[0], tot);
+    {
+      // validation: order-free reductions, one shared atomic per warp and chunk
+      // (after the scan's barriers, so after thread 0 cleared the sums)
+      long long wl = len;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
+      const int wb = (int)__reduce_or_sync(0xffffffffu, (unsigned)bad);
+      if (lane == 0) {
+        if (wb) atomicOr(&bad_sh, wb);
+        if (wl) atomicAdd(&len_sh, (unsigned long long)wl);
+      }
+    }
     if (s < S) {
       s_start[s] = carry + ex;
       p.seq_start[s] = carry + ex;
@@ -252,11 +276,47 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
       s_key[s] = key < 0 ? -1 : (key | (lead << kLeadShift));
     }
     carry += tot;
+    if (p.tables) {
+      // stable ranks of this chunk: each warp's per-key totals go to its row
+      // of the tables; a sequence adds the rows of the earlier warps and the
+      // running counts of the earlier chunks; then the counts advance
+      const bool tc = key >= N;
+      const int id = tc ? key - N : key;
+      for (int i = tid; i < kSegWarps * 3 * N; i += kSegThreads) tab_rows[i] = 0;
+      __syncthreads();
+      if (key >= 0 && lead == lane) {
+        tab_rows[warp * 2 * N + key] = pl + len;
+        if (tc) tab_tiles[warp * N + id] = pt + nt;
+      }
+      __syncthreads();
+      if (key >= 0) {
+        int br = run_tok[key], bt = tc ? cnt_tile[id] : 0;
+        for (int w = 0; w < warp; ++w) {
+          br += tab_rows[w * 2 * N + key];
+          if (tc) bt += tab_tiles[w * N + id];
+        }
+        s_pos[s] = br + pl;
+        if (tc) s_tile[s] = bt + pt;
+      }
+      __syncthreads();  // every read of the running counts is done
+      for (int k = tid; k < 2 * N; k += kSegThreads) {
+        int add = 0;
+#pragma unroll
+        for (int w = 0; w < kSegWarps; ++w) add += tab_rows[w * 2 * N + k];
+        run_tok[k] += add;
+      }
+      for (int k = tid; k < N; k += kSegThreads) {
+        int add = 0;
+#pragma unroll
+        for (int w = 0; w < kSegWarps; ++w) add += tab_tiles[w * N + k];
+        cnt_tile[k] += add;
+      }
+      // the next chunk's block scan has barriers before its tables are cleared
+    }
   }
-  // validation: order-free reductions
-  if (bad) atomicOr(&bad_sh, bad);
-  if (my_len) atomicAdd(&len_sh, (unsigned long long)my_len);
-  __syncthreads();
+  // the validation sums are complete: with the tables, barriers in the loop
+  // follow every chunk's atomics; without them, this one
+  if (!p.tables || S == 0) __syncthreads();
   {
     const int bb = bad_sh;
     if ((bb & 1) || len_sh != (unsigned long long)(long long)T || (bb & 2)) {
@@ -268,28 +328,14 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   }
   if (tid == 0) p.seq_start[S] = T;
 
-  // ---- stable ranks: one warp walks the sequences 32 at a time in index
-  // order (the next chunk's entries are read ahead); the per-key running
-  // counts end as the rows per (class, slot) and the tiles per slot
-  if (warp == 0) {
-    auto fetch = [&](int s, int& kk, int& pl, int& pt, int& len) {
-      if (s < S) {
-        kk = s_key[s];
-        pl = s_pos[s];
-        pt = s_tile[s];
-        len = s_len[s];
-      } else {
-        kk = -1;
-        pl = pt = len = 0;
-      }
-    };
-    int kk, pl, pt, len;
-    fetch(lane, kk, pl, pt, len);
+  // ---- stable ranks (without the tables): one warp walks the sequences 32
+  // at a time in index order; the per-key running counts end as the rows per
+  // (class, slot) and the tiles per slot
+  if (!p.tables && warp == 0) {
     for (int b = 0; b < S; b += 32) {
-      int kk2, pl2, pt2, len2;
-      fetch(b + 32 + lane, kk2, pl2, pt2, len2);
-      const int s = b + lane;
-      const bool act = kk >= 0;
+      const int s = b + lane, sc = min(s, S - 1);
+      const int kk = s_key[sc], pl = s_pos[sc], pt = s_tile[sc], len = s_len[sc];
+      const bool act = s < S && kk >= 0;
       const int key = act ? (kk & kKeyMask) : 0;
       const int lead = act ? (kk >> kLeadShift) : lane;
       const bool tc = key >= N, last = act && lead == lane;
@@ -312,24 +358,14 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
         if (tc) cnt_tile[id] = base_tile + pt + (len + kTcTile - 1) / kTcTile;
       }
       __syncwarp();  // this chunk's counts are visible to the next chunk's reads
-      kk = kk2;
-      pl = pl2;
-      pt = pt2;
-      len = len2;
     }
   }
   __syncthreads();
 
   // ---- offsets: rows (class-major), decode groups per slot, tiles per slot
-  for (int i = tid; i < 2 * N; i += kSegThreads) cnt_tok[i] = run_tok[i];
-  for (int k = tid; k < N; k += kSegThreads) {
-    dec_cnt[k] = (run_tok[k] + kDecGroup - 1) / kDecGroup;
-    tc_cnt[k] = cnt_tile[k];
-  }
-  __syncthreads();
   int n_active, n_dec_work, n_tc;
-  block_scan3(cnt_tok, 2 * N, dec_cnt, N, tc_cnt, N, (2 * N + kSegThreads - 1) / kSegThreads, scan_sums, n_active,
-              n_dec_work, n_tc);
+  block_scan3(run_tok, cnt_tok, 2 * N, dec_cnt, N, cnt_tile, tc_cnt, N, (2 * N + kSegThreads - 1) / kSegThreads,
+              scan_sums, n_active, n_dec_work, n_tc);
   if (tid == 0) {
     dec_cnt[N] = n_dec_work;
     tc_cnt[N] = n_tc;
@@ -499,11 +535,14 @@ int launch_seg_build(lora_segments* seg, const int32_t* ids, const int32_t* lens
   p.dec_rows = seg->dec_rows;
   p.tc_work = seg->tc_work;
   p.seq_scratch = seg->seq_scratch;
-  p.seq_smem = seq_arrays_in_smem(seg->N, S) ? 1 : 0;
-  const size_t sm = sizeof(int) * (seg_key_ints(seg->N) + (p.seq_smem ? 6 * (size_t)S : 0));
-  if (sm > 48 * 1024 && !set_smem_limit(reinterpret_cast<const void*>(seg_build_kernel), seg->device, (int)sm))
+  const bool in_smem = seq_arrays_in_smem(seg->N, S);
+  size_t sm = sizeof(int) * (seg_key_ints(seg->N) + (in_smem ? 6 * (size_t)S : 0));
+  p.tables = sm + sizeof(int) * seg_table_ints(seg->N) <= kSegSmemLimit ? 1 : 0;
+  if (p.tables) sm += sizeof(int) * seg_table_ints(seg->N);
+  auto kern = in_smem ? seg_build_kernel<true> : seg_build_kernel<false>;
+  if (sm > 48 * 1024 && !set_smem_limit(reinterpret_cast<const void*>(kern), seg->device, (int)sm))
     return LORA_ERR_CUDA;
-  const cudaError_t e = launch_pdl(seg_build_kernel, dim3(1), dim3(kSegThreads), sm, st, p);
+  const cudaError_t e = launch_pdl(kern, dim3(1), dim3(kSegThreads), sm, st, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(e != cudaSuccess ? e : cudaGetLastError(), "seg_build_kernel launch");
 }

@@ -52,12 +52,13 @@ constexpr int kFpStageBytes = kFpXBytes + kFpN * kFpK * 2;    // 48 KB
 constexpr int kFpGroups = 2;                                  // 16-rank groups per expand step
 constexpr int kFpBkGroupBytes = kFpN * 32;                    // B of 256 columns x 16 ranks
 constexpr int kFpUGroupBytes = kFpM * 32;                     // u' of 128 rows x 16 ranks
-constexpr int kFpUHi = kFpGroups * kFpBkGroupBytes;           // offsets inside an expand stage
-constexpr int kFpULo = kFpUHi + kFpGroups * kFpUGroupBytes;
-constexpr int kFpThreads = 192;
+constexpr int kFpUBufs = 2;                                   // u' operand buffers (hi then lo halves)
+constexpr int kFpUBufBytes = 2 * kFpGroups * kFpUGroupBytes;  // 16 KB
+constexpr int kFpThreads = 320;                               // TMA, MMA, 4 operand warps, 4 epilogue warps
 constexpr int kFpBandTiles = 8;                               // row tiles per band of the tile order
 constexpr int kFpSlotWords = LORA_MAX_SLOTS / 32;
-static_assert(kFpULo + kFpGroups * kFpUGroupBytes <= kFpStageBytes, "an expand step fits a stage");
+constexpr int kFpSmem = kFpStages * kFpStageBytes + kFpUBufs * kFpUBufBytes + 1024;
+static_assert(kFpGroups * kFpBkGroupBytes <= kFpStageBytes, "an expand step's B fits a stage");
 
 struct FpParams {
   const int32_t* slot;  // [T] per-token slot (segment builder)
@@ -66,7 +67,7 @@ struct FpParams {
   float* y;
   int32_t* status;
   int64_t ldy;
-  int T, D, nkb, L, R16, N, ntm, ntn;
+  int T, D, nkb, L, R16, N, ntm, ntn, ntiles;
   int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES];
 };
 
@@ -76,7 +77,7 @@ struct FpParams {
 // lane columns [lc0, lc0 + c_w).  f returns false to stop.  Every role runs
 // its own walk over the same shared list and tables, so all agree.
 template <typename F>
-__device__ __forceinline__ void for_each_step(const FpParams& p, const int* slots, int nslots, int n0, F&& f) {
+__device__ __forceinline__ bool for_each_step(const FpParams& p, const int* slots, int nslots, int n0, F&& f) {
   for (int j = 0; j < nslots; ++j) {
     const int k = slots[j];
 #pragma unroll
@@ -88,53 +89,71 @@ __device__ __forceinline__ void for_each_step(const FpParams& p, const int* slot
       if (r <= 0) continue;
       const int nk = (r + 15) / 16;
       for (int q0 = 0; q0 < nk; q0 += kFpGroups)
-        if (!f(k, l, q0, min(kFpGroups, nk - q0), lo - n0, hi - lo, lo - p.off[l])) return;
+        if (!f(k, l, q0, min(kFpGroups, nk - q0), lo - n0, hi - lo, lo - p.off[l])) return false;
     }
   }
+  return true;
+}
+
+// Tile t of the order: bands of kFpBandTiles row tiles, column tiles in order
+// inside a band (CTAs working at the same time share W and x tiles in L2).
+__device__ __forceinline__ void tile_origin(const FpParams& p, int t, int& m0, int& n0) {
+  const int band_size = kFpBandTiles * p.ntn;
+  const int band = t / band_size, in_band = t - band * band_size;
+  const int rows_in_band = min(kFpBandTiles, p.ntm - band * kFpBandTiles);
+  m0 = (band * kFpBandTiles + in_band % rows_in_band) * kFpM;
+  n0 = (in_band / rows_in_band) * kFpN;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Persistent: CTA b takes tiles b, b + G, b + 2G, ... (G = the grid).  Two
+// accumulators of 256 TMEM columns alternate between tiles, so the epilogue of
+// one tile runs while the next one's K loop does.  Every barrier a role waits
+// on is waited on phase by phase, in order, by that role.
 __global__ void __launch_bounds__(kFpThreads, 1)
     fused_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ TmapSized tm_bk, FpParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kFpStages], empty_bar[kFpStages], ufull_bar[kFpStages];
-  __shared__ __align__(8) uint64_t plan_bar, main_bar, done_bar;
+  __shared__ __align__(8) uint64_t full_bar[kFpStages], empty_bar[kFpStages];
+  __shared__ __align__(8) uint64_t ufull_bar[kFpUBufs], uempty_bar[kFpUBufs];
+  __shared__ __align__(8) uint64_t plan_full[2], plan_empty[2], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int fail_sh, nslots_sh;
+  __shared__ int fail_sh;
+  __shared__ int nslots_sh[2];
+  __shared__ int stop_sh[2];  // per plan buffer: a warp of warps 2-5 saw a failure (they stop together)
+  __shared__ int slots_sh[2][kFpM];
   __shared__ uint32_t bits_sh[kFpSlotWords];
-  __shared__ int slots_sh[kFpM];
 
   pdl_wait();  // the shrinks' u' (and the builder's slots) are visible from here on
   if (*p.status != 0) return;  // a routing error or an earlier timeout: y is not written
 
-  // tile order: bands of kFpBandTiles row tiles, column tiles in order inside a band
-  const int band_size = kFpBandTiles * p.ntn;
-  const int band = blockIdx.x / band_size, in_band = blockIdx.x - band * band_size;
-  const int rows_in_band = min(kFpBandTiles, p.ntm - band * kFpBandTiles);
-  const int m0 = (band * kFpBandTiles + in_band % rows_in_band) * kFpM;
-  const int n0 = (in_band / rows_in_band) * kFpN;
-
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ubuf = smem + kFpStages * kFpStageBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFpStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
-      mbar_init(&ufull_bar[s], 4);
     }
-    mbar_init(&plan_bar, 1);
-    mbar_init(&main_bar, 1);
-    mbar_init(&done_bar, 1);
+    for (int q = 0; q < kFpUBufs; ++q) {
+      mbar_init(&ufull_bar[q], 4);
+      mbar_init(&uempty_bar[q], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&plan_full[b], 1);
+      mbar_init(&plan_empty[b], 2);
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
     fail_sh = 0;
-    nslots_sh = 0;
+    stop_sh[0] = stop_sh[1] = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_base_sh, kFpN);
+    tmem_alloc(&tmem_base_sh, 2 * kFpN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -157,20 +176,25 @@ __global__ void __launch_bounds__(kFpThreads, 1)
         mbar_expect_tx(&full_bar[s], bytes);
         return smem + (size_t)s * kFpStageBytes;
       };
-      for (int kb = 0; kb < p.nkb && ok; ++kb) {
-        uint8_t* st = take((uint32_t)kFpStageBytes);
-        if (!st) break;
-        uint64_t* fb = &full_bar[i % kFpStages];
-        tma_load_2d(st, &tm_x, kb * kFpK, m0, fb);
-        tma_load_2d(st + kFpXBytes, &tm_w, kb * kFpK, n0, fb);
-        ++i;
-      }
-      if (ok && !mbar_wait_or_fail(&plan_bar, 0, &fail_sh)) {
-        fail_sh = 1;
-        ok = false;
-      }
-      if (ok) {
-        for_each_step(p, slots_sh, nslots_sh, n0, [&](int k, int l, int q0, int ng, int, int c_w, int lc0) {
+      int jj = 0;
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x, ++jj) {
+        int m0, n0;
+        tile_origin(p, t, m0, n0);
+        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+          uint8_t* st = take((uint32_t)kFpStageBytes);
+          if (!st) break;
+          uint64_t* fb = &full_bar[i % kFpStages];
+          tma_load_2d(st, &tm_x, kb * kFpK, m0, fb);
+          tma_load_2d(st + kFpXBytes, &tm_w, kb * kFpK, n0, fb);
+          ++i;
+        }
+        const int b = jj & 1;
+        if (ok && !mbar_wait_or_fail(&plan_full[b], (jj >> 1) & 1, &fail_sh)) {
+          fail_sh = 1;
+          ok = false;
+        }
+        if (!ok) break;
+        for_each_step(p, slots_sh[b], nslots_sh[b], n0, [&](int k, int l, int q0, int ng, int, int c_w, int lc0) {
           const int nb = (c_w + 127) / 128;  // boxes of 128 columns per group
           uint8_t* st = take((uint32_t)(ng * nb * 4096));
           if (!st) return false;
@@ -182,6 +206,7 @@ __global__ void __launch_bounds__(kFpThreads, 1)
           ++i;
           return true;
         });
+        if (ok) mbar_arrive(&plan_empty[b]);
       }
       // Copies already issued land before the CTA may leave (after a failure
       // the MMA thread may not have waited for them): the latest fill of
@@ -192,192 +217,215 @@ __global__ void __launch_bounds__(kFpThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      uint32_t i = 0;
+      uint32_t i = 0, n = 0;  // ring stage uses, u' buffer uses
       bool ok = true;
       const uint32_t idesc_main = idesc_bf16(kFpM, kFpN);
-      for (int kb = 0; kb < p.nkb; ++kb, ++i) {
-        const int s = (int)(i % kFpStages);
-        if (!mbar_wait_or_fail(&full_bar[s], (i / kFpStages) & 1, &fail_sh)) {
+      int jj = 0;
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x, ++jj) {
+        int m0, n0;
+        tile_origin(p, t, m0, n0);
+        const int b = jj & 1;
+        const uint32_t acc = tmem + (uint32_t)(b * kFpN);
+        if (jj >= 2 && !mbar_wait_or_fail(&acc_empty[b], ((jj >> 1) - 1) & 1, &fail_sh)) {
           fail_sh = 1;
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t xa = smem_u32(smem + (size_t)s * kFpStageBytes), wa = xa + kFpXBytes;
-#pragma unroll
-        for (int kk = 0; kk < kFpK / 16; ++kk)
-          mma_bf16(tmem, smem_desc(xa + 32 * kk, 16, 1024, kSwz128), smem_desc(wa + 32 * kk, 16, 1024, kSwz128),
-                   idesc_main, (kb | kk) != 0 ? 1u : 0u);
-        mma_commit(&empty_bar[s]);
-      }
-      if (ok) mma_commit(&main_bar);  // every stage's K-loop uses are done once this arrives
-      if (ok && !mbar_wait_or_fail(&plan_bar, 0, &fail_sh)) {
-        fail_sh = 1;
-        ok = false;
-      }
-      if (ok) {
-        uint32_t upar = 0;  // bit s: parity of the next u' fill of stage s
-        for_each_step(p, slots_sh, nslots_sh, n0, [&](int, int, int, int ng, int c_lo, int c_w, int) {
+        for (int kb = 0; kb < p.nkb; ++kb, ++i) {
           const int s = (int)(i % kFpStages);
-          if (!mbar_wait_or_fail(&full_bar[s], (i / kFpStages) & 1, &fail_sh) ||
-              !mbar_wait_or_fail(&ufull_bar[s], (upar >> s) & 1u, &fail_sh)) {
+          if (!mbar_wait_or_fail(&full_bar[s], (i / kFpStages) & 1, &fail_sh)) {
             fail_sh = 1;
             ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xa = smem_u32(smem + (size_t)s * kFpStageBytes), wa = xa + kFpXBytes;
+#pragma unroll
+          for (int kk = 0; kk < kFpK / 16; ++kk)
+            mma_bf16(acc, smem_desc(xa + 32 * kk, 16, 1024, kSwz128), smem_desc(wa + 32 * kk, 16, 1024, kSwz128),
+                     idesc_main, (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(&empty_bar[s]);
+        }
+        if (ok && !mbar_wait_or_fail(&plan_full[b], (jj >> 1) & 1, &fail_sh)) {
+          fail_sh = 1;
+          ok = false;
+        }
+        if (!ok) break;
+        ok = for_each_step(p, slots_sh[b], nslots_sh[b], n0, [&](int, int, int, int ng, int c_lo, int c_w, int) {
+          const int s = (int)(i % kFpStages), q = (int)(n % kFpUBufs);
+          if (!mbar_wait_or_fail(&full_bar[s], (i / kFpStages) & 1, &fail_sh) ||
+              !mbar_wait_or_fail(&ufull_bar[q], (n / kFpUBufs) & 1, &fail_sh)) {
+            fail_sh = 1;
             return false;
           }
-          upar ^= 1u << s;
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)s * kFpStageBytes);
+          const uint32_t ua = smem_u32(ubuf + (size_t)q * kFpUBufBytes);
           const uint32_t idesc = idesc_bf16(kFpM, c_w);
-          const uint32_t d = tmem + (uint32_t)c_lo;
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t ua = sa + (half ? kFpULo : kFpUHi);
+          for (int half = 0; half < 2; ++half)
             for (int g = 0; g < ng; ++g)
-              mma_bf16(d, smem_desc(ua + g * kFpUGroupBytes, 128, 256, kSwzNone),
+              mma_bf16(acc + (uint32_t)c_lo,
+                       smem_desc(ua + (half * kFpGroups + g) * kFpUGroupBytes, 128, 256, kSwzNone),
                        smem_desc(sa + g * kFpBkGroupBytes, 16, 256, kSwz32), idesc, 1u);
-          }
           mma_commit(&empty_bar[s]);
+          mma_commit(&uempty_bar[q]);
           ++i;
+          ++n;
           return true;
         });
+        if (!ok) break;
+        mma_commit(&acc_full[b]);
+        mbar_arrive(&plan_empty[b]);
       }
-      if (ok) mma_commit(&done_bar);
     }
-  } else {
-    // ---------------- warps 2-5: the tile's slots, the u' operands, the epilogue
-    const int quad = warp & 3;
-    const int m = quad * 32 + lane;  // this thread's tile row = its TMEM lane
-    const int t = m0 + m;
+  } else if (warp < 6) {
+    // ---------------- warps 2-5: each tile's slots, then the u' operands of
+    // its expand steps: row m of the slot's rows, zero for rows of other
+    // slots, as bf16 hi and lo in the K-major core-matrix layout (8 rows x 16
+    // bytes per core matrix; 16 ranks = two of them)
+    const int m = (warp & 3) * 32 + lane;
     const int bt = threadIdx.x - 64;  // 0..127
-    const int myslot = t < p.T ? p.slot[t] : 0;
-    for (int w = bt; w < kFpSlotWords; w += 128) bits_sh[w] = 0u;
-    named_bar_sync(1, 128);
-    if (myslot > 0) atomicOr(&bits_sh[myslot >> 5], 1u << (myslot & 31));
-    named_bar_sync(1, 128);
-    if (warp == 2) {
-      // distinct slots of the tile in ascending order
-      const int nw = (p.N + 31) / 32;
-      uint32_t w0 = 2 * lane < nw ? bits_sh[2 * lane] : 0u, w1 = 2 * lane + 1 < nw ? bits_sh[2 * lane + 1] : 0u;
-      const int c = __popc(w0) + __popc(w1);
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int pos = incl - c;
-      while (w0) {
-        slots_sh[pos++] = 64 * lane + __ffs(w0) - 1;
-        w0 &= w0 - 1;
-      }
-      while (w1) {
-        slots_sh[pos++] = 64 * lane + 32 + __ffs(w1) - 1;
-        w1 &= w1 - 1;
-      }
-      if (lane == 31) nslots_sh = incl;
-    }
-    named_bar_sync(1, 128);
-    if (warp == 2 && lane == 0) mbar_arrive(&plan_bar);
-
-    // u' operands of the expand steps: row m of the slot's rows, zero for
-    // rows of other slots, as bf16 hi and lo in the K-major core-matrix
-    // layout (8 rows x 16 bytes per core matrix; 16 ranks = two of them)
-    // A parity wait names one of two phases, so it is only sound while the
-    // barrier is at most one phase behind the awaited one.  These warps skip
-    // the K loop's stage uses; they start once its MMAs are complete, and from
-    // then on wait for every expand use of a stage in order.
-    bool ok = true;
-    {
-      int got = 1;
-      if (nslots_sh > 0 && lane == 0) got = mbar_wait_or_fail(&main_bar, 0, &fail_sh) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, got, 0)) {
-        fail_sh = 1;
-        ok = false;
-      }
-    }
-    uint32_t i = (uint32_t)p.nkb;
     const uint32_t row_off = (uint32_t)((m >> 3) * 256 + (m & 7) * 16);
-    if (ok) for_each_step(p, slots_sh, nslots_sh, n0, [&](int k, int l, int q0, int ng, int, int, int) {
-      const int s = (int)(i % kFpStages);
-      if (i >= kFpStages) {  // one lane waits for the stage to be free; the warp follows it
+    // These four warps meet at named barriers, so they leave the tile loop
+    // together: a failure any of them sees goes into stop_sh[b] between the
+    // first and the third barrier of a tile, and all read it after the third.
+    uint32_t n = 0;
+    bool ok = true;
+    int jj = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++jj) {
+      int m0, n0;
+      tile_origin(p, t, m0, n0);
+      const int b = jj & 1;
+      const int tr = m0 + m;
+      const int myslot = tr < p.T ? p.slot[tr] : 0;
+      if (ok && jj >= 2) {  // the plan buffer is free once the producer and the MMA thread are done with it
         int got = 1;
-        if (lane == 0) got = mbar_wait_or_fail(&empty_bar[s], ((i / kFpStages) - 1) & 1, &fail_sh) ? 1 : 0;
+        if (lane == 0) got = mbar_wait_or_fail(&plan_empty[b], ((jj >> 1) - 1) & 1, &fail_sh) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, got, 0)) {
           fail_sh = 1;
           ok = false;
-          return false;
         }
       }
-      uint8_t* st = smem + (size_t)s * kFpStageBytes;
-      const bool mine = myslot == k;
-      const float4* src =
-          reinterpret_cast<const float4*>(p.u_rows + ((size_t)(mine ? t : 0) * p.L + l) * p.R16 + 16 * q0);
-      for (int g = 0; g < ng; ++g) {
-        float u[16];
+      if (bt == 0) stop_sh[b] = 0;  // every warp read it two tiles ago, before the barriers of the last tile
+      for (int w = bt; w < kFpSlotWords; w += 128) bits_sh[w] = 0u;
+      named_bar_sync(1, 128);
+      if (lane == 0 && (!ok || fail_sh)) atomicOr(&stop_sh[b], 1);
+      if (myslot > 0) atomicOr(&bits_sh[myslot >> 5], 1u << (myslot & 31));
+      named_bar_sync(1, 128);
+      if (warp == 2) {
+        // distinct slots of the tile in ascending order
+        const int nw = (p.N + 31) / 32;
+        uint32_t w0 = 2 * lane < nw ? bits_sh[2 * lane] : 0u, w1 = 2 * lane + 1 < nw ? bits_sh[2 * lane + 1] : 0u;
+        const int c = __popc(w0) + __popc(w1);
+        int incl = c;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 v = mine ? __ldcg(src + 4 * g + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-          u[4 * e] = v.x;
-          u[4 * e + 1] = v.y;
-          u[4 * e + 2] = v.z;
-          u[4 * e + 3] = v.w;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
         }
-#pragma unroll
-        for (int kc = 0; kc < 2; ++kc) {
-          uint32_t hw[4], lw[4];
+        int pos = incl - c;
+        while (w0) {
+          slots_sh[b][pos++] = 64 * lane + __ffs(w0) - 1;
+          w0 &= w0 - 1;
+        }
+        while (w1) {
+          slots_sh[b][pos++] = 64 * lane + 32 + __ffs(w1) - 1;
+          w1 &= w1 - 1;
+        }
+        if (lane == 31) nslots_sh[b] = incl;
+      }
+      named_bar_sync(1, 128);
+      if (stop_sh[b]) break;
+      if (warp == 2 && lane == 0) mbar_arrive(&plan_full[b]);
+      ok = for_each_step(p, slots_sh[b], nslots_sh[b], n0, [&](int k, int l, int q0, int ng, int, int, int) {
+        const int q = (int)(n % kFpUBufs);
+        if (n >= kFpUBufs) {  // one lane waits for the buffer to be free; the warp follows it
+          int got = 1;
+          if (lane == 0) got = mbar_wait_or_fail(&uempty_bar[q], ((n / kFpUBufs) - 1) & 1, &fail_sh) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, got, 0)) {
+            fail_sh = 1;
+            return false;
+          }
+        }
+        uint8_t* ub = ubuf + (size_t)q * kFpUBufBytes;
+        const bool mine = myslot == k;
+        const float4* src =
+            reinterpret_cast<const float4*>(p.u_rows + ((size_t)(mine ? tr : 0) * p.L + l) * p.R16 + 16 * q0);
+        for (int g = 0; g < ng; ++g) {
+          float u[16];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float u0 = u[8 * kc + 2 * e], u1 = u[8 * kc + 2 * e + 1];
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(u0), h1 = __float2bfloat16_rn(u1);
-            const __nv_bfloat16 l0 = __float2bfloat16_rn(u0 - __bfloat162float(h0));
-            const __nv_bfloat16 l1 = __float2bfloat16_rn(u1 - __bfloat162float(h1));
-            hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-            lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+            const float4 v = mine ? __ldcg(src + 4 * g + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            u[4 * e] = v.x;
+            u[4 * e + 1] = v.y;
+            u[4 * e + 2] = v.z;
+            u[4 * e + 3] = v.w;
           }
-          const uint32_t o = (uint32_t)(g * kFpUGroupBytes + kc * 128) + row_off;
-          *reinterpret_cast<uint4*>(st + kFpUHi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(st + kFpULo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+          for (int kc = 0; kc < 2; ++kc) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float u0 = u[8 * kc + 2 * e], u1 = u[8 * kc + 2 * e + 1];
+              const __nv_bfloat16 h0 = __float2bfloat16_rn(u0), h1 = __float2bfloat16_rn(u1);
+              const __nv_bfloat16 l0 = __float2bfloat16_rn(u0 - __bfloat162float(h0));
+              const __nv_bfloat16 l1 = __float2bfloat16_rn(u1 - __bfloat162float(h1));
+              hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+              lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+            }
+            const uint32_t o = (uint32_t)(g * kFpUGroupBytes + kc * 128) + row_off;
+            *reinterpret_cast<uint4*>(ub + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(ub + kFpGroups * kFpUGroupBytes + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
         }
-      }
-      fence_proxy_async_smem();  // the MMA reads these through the async proxy
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ufull_bar[s]);
-      ++i;
-      return true;
-    });
-
-    // epilogue: this thread's row of the tile, 32 columns at a time (ok is
-    // uniform over the warp: the tcgen05.ld below is warp-collective)
-    if (ok) {
-      int got = 1;
-      if (lane == 0) got = mbar_wait_or_fail(&done_bar, 0, &fail_sh) ? 1 : 0;
+        fence_proxy_async_smem();  // the MMA reads these through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ufull_bar[q]);
+        ++n;
+        return true;
+      });
+    }
+  } else {
+    // ---------------- warps 6-9: epilogue, one tile row per thread, 32
+    // columns at a time; the accumulator goes back to the MMA thread after
+    const int quad = warp & 3;
+    const int m = quad * 32 + lane;
+    const uint32_t trow = (uint32_t)(quad * 32) << 16;
+    int jj = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++jj) {
+      int m0, n0;
+      tile_origin(p, t, m0, n0);
+      const int b = jj & 1;
+      int got = 1;  // uniform over the warp: the tcgen05.ld below is warp-collective
+      if (lane == 0) got = mbar_wait_or_fail(&acc_full[b], (jj >> 1) & 1, &fail_sh) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, got, 0)) {
         fail_sh = 1;
-        ok = false;
-      } else {
-        tc_fence_after();
+        break;
       }
-    }
-    if (ok) {
-      const uint32_t trow = (uint32_t)(quad * 32) << 16;
-      float* yr = p.y + (size_t)t * p.ldy + n0;
+      tc_fence_after();
+      const int tr = m0 + m;
+      float* yr = p.y + (size_t)tr * p.ldy + n0;
 #pragma unroll 1
       for (int j = 0; j < kFpN / 32; ++j) {
         float v[32];
-        tmem_ld32(tmem + trow + (uint32_t)(32 * j), v);
-        if (t < p.T && n0 + 32 * j < p.D) {
+        tmem_ld32(tmem + trow + (uint32_t)(b * kFpN + 32 * j), v);
+        if (tr < p.T && n0 + 32 * j < p.D) {
           float4* dst = reinterpret_cast<float4*>(yr + 32 * j);
 #pragma unroll
           for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kFpN);
+    tmem_dealloc(tmem, 2 * kFpN);
   }
   if (threadIdx.x == 0 && fail_sh) set_error(p.status, LORA_ERR_TIMEOUT);
 }
@@ -420,13 +468,14 @@ int launch_fused_projection(const PoolView& pool, const lora_segments* seg, cons
   p.N = pool.N;
   p.ntm = ceil_div(T, kFpM);
   p.ntn = ceil_div(pool.D, kFpN);
+  p.ntiles = p.ntm * p.ntn;
   for (int l = 0; l < LORA_MAX_LANES; ++l) {
     p.d_out[l] = pool.d_out[l];
     p.off[l] = pool.off[l];
   }
-  const long long grid = (long long)p.ntm * p.ntn;
-  if (grid > 0x7fffffffLL) return LORA_ERR_SHAPE;
-  const int smem = kFpStages * kFpStageBytes + 1024;
+  if ((long long)p.ntm * p.ntn > 0x7fffffffLL) return LORA_ERR_SHAPE;
+  const int grid = p.ntiles < sm_count(pool.device) ? p.ntiles : sm_count(pool.device);  // one CTA per SM
+  const int smem = kFpSmem;
   if (!set_smem_limit(reinterpret_cast<const void*>(fused_proj_kernel), pool.device, smem)) return LORA_ERR_CUDA;
   const cudaError_t e =
       launch_pdl(fused_proj_kernel, dim3((unsigned)grid), dim3(kFpThreads), smem, st, tm_x, tm_w, pool.tm_bk, p);

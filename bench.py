@@ -185,7 +185,8 @@ def traffic_from_profile(kernel: str, workload: str):
             vals[k.strip()] = v.strip()
     src = os.path.join(ROOT, "adapter_gemv_lora_gb300", "csrc",
                        "tensor.cu" if kernel.startswith("tc_") else
-                       "segments.cu" if kernel.startswith("seg_") else "decode.cu")
+                       "segments.cu" if kernel.startswith("seg_") else
+                       "fused.cu" if kernel.startswith("fused_") else "decode.cu")
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     if vals.get("source_sha256_16") != sha:
         return None
@@ -739,6 +740,21 @@ def workload_record(wl, res, hbm_peak, bf16_peak):
             "kernels": kernels}
 
 
+def run_fused_only(args):
+    """The fused projection of one workload alone (a diagnostic line, e.g.
+    for a profiler capture on a smaller case via --max-seqs)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device("cuda:0")
+    wl = W.make_workload(args.workload, seed=args.seed)
+    if args.max_seqs:
+        wl = truncate_workload(wl, args.max_seqs)
+    hbm_peak, bf16_peak, _ = measured_peaks()
+    rec = fused_record(wl, time_fused(wl, args.steps, args.warmup, "cuda:0"), bf16_peak, hbm_peak)
+    print(json.dumps({"mode": "fused_projection", "workload": wl.name, "tokens": wl.T, **rec}), flush=True)
+
+
 def run_ours(args):
     import torch
     ws, rank, local = dist_env()
@@ -929,6 +945,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--headline-only", action="store_true", help="skip the per_workload records of all configs")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused-projection records")
+    ap.add_argument("--fused-only", action="store_true",
+                    help="time only the fused projection of --workload (one diagnostic JSON line)")
     ap.add_argument("--only", default="", help="per_workload: only these comma-separated configurations")
     ap.add_argument("--max-seqs", type=int, default=0,
                     help="keep only the first N sequences of the workload (smaller case for profiler captures)")
@@ -937,6 +955,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.fused_only:
+        run_fused_only(args)
     else:
         run_ours(args)
 

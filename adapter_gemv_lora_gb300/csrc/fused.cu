@@ -55,7 +55,7 @@ constexpr int kFpUGroupBytes = kFpM * 32;                     // u' of 128 rows 
 constexpr int kFpUBufs = 2;                                   // u' operand buffers (hi then lo halves)
 constexpr int kFpUBufBytes = 2 * kFpGroups * kFpUGroupBytes;  // 16 KB
 constexpr int kFpThreads = 320;                               // TMA, MMA, 4 operand warps, 4 epilogue warps
-constexpr int kFpBandTiles = 8;                               // row tiles per band of the tile order
+constexpr int kFpBandTiles = 16;                              // row tiles per band of the tile order
 constexpr int kFpSlotWords = LORA_MAX_SLOTS / 32;
 constexpr int kFpSmem = kFpStages * kFpStageBytes + kFpUBufs * kFpUBufBytes + 1024;
 static_assert(kFpGroups * kFpBkGroupBytes <= kFpStageBytes, "an expand step's B fits a stage");

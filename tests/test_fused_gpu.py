@@ -240,3 +240,51 @@ def test_fused_host_checks():
                                            yd.data_ptr(), proj.d_in, proj.D, None) == LD.LORA_ERR_ARG
     assert lib.lora_fused_projection_stage(pool.handle, seg.handle, wd.data_ptr(), proj.d_in, xd.data_ptr(),
                                            yd.data_ptr(), proj.d_in, proj.D, 4, None) == LD.LORA_ERR_ARG
+
+
+def test_fused_one_graph_serves_any_adapter_mixture(oracle_mod):
+    # build + fused projection captured once, replayed for other adapter ids
+    # and other length splits of the same totals (decode and prompt rows)
+    from adapter_gemv_lora_gb300 import lora_delta as LD
+    torch = TL.torch_mod()
+    lens0 = [1, 200, 1, 3, 129, 64, 1, 2]
+    ids0 = [1, 2, 0, 3, 4, 1, 4, 2]
+    wl = W.custom_workload(lens0, ids0, d_in=512, lane_d_out=[256, 128], num_slots=5, max_rank=32, seed=12)
+    proj = wl.projections[0]
+    Wb = W.projection_weight(proj)
+    pool = TL.build_pool(proj, wl.T)
+    seg = LD.LoraSegments(wl.S, wl.T, wl.num_slots, device="cuda")
+    ids = torch.tensor(wl.adapter_ids, dtype=torch.int32, device="cuda")
+    lens = torch.tensor(wl.q_seq_lens, dtype=torch.int32, device="cuda")
+    x = TL.to_dev_u16(proj.x)
+    wd = TL.to_dev_u16(Wb)
+    y = torch.zeros((wl.T, proj.D), device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s_ = torch.cuda.Stream()
+    s_.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_):
+        seg.build(ids, lens, num_tokens=wl.T)  # one eager step before capture
+        LD.fused_projection(pool, seg, wd, x, y)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            seg.build(ids, lens, num_tokens=wl.T)
+            LD.fused_projection(pool, seg, wd, x, y)
+    torch.cuda.current_stream().wait_stream(s_)
+    rng = np.random.default_rng(21)
+    base, mag = oracle_mod.base_product(Wb, proj.x)
+    for mix in range(3):
+        new_ids = rng.integers(0, wl.num_slots, size=wl.S).astype(np.int32)
+        cut = np.sort(rng.choice(np.arange(1, wl.T), size=wl.S - 1, replace=False))
+        new_lens = np.diff(np.concatenate([[0], cut, [wl.T]])).astype(np.int32)
+        ids.copy_(torch.from_numpy(new_ids))
+        lens.copy_(torch.from_numpy(new_lens))
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert seg.status() == 0
+        slot = np.repeat(new_ids, new_lens)
+        _, dref = oracle_mod.delta(proj, slot)
+        got = y.cpu().numpy().astype(np.float64)
+        err = np.abs(got - (base + dref))
+        tol = TL.ATOL + TL.RTOL * np.abs(dref) + proj.d_in * 2.0 ** -23 * mag
+        assert np.all(err <= tol), f"mixture {mix}: {int((err > tol).sum())} elements out of tolerance"

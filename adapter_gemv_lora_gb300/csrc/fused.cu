@@ -340,6 +340,16 @@ __global__ void __launch_bounds__(kFpThreads, 1)
       if (warp == 2 && lane == 0) mbar_arrive(&plan_full[b]);
       ok = for_each_step(p, slots_sh[b], nslots_sh[b], n0, [&](int k, int l, int q0, int ng, int, int, int) {
         const int q = (int)(n % kFpUBufs);
+        const bool mine = myslot == k;
+        // this row's u' first, so the loads are in flight during the wait
+        const float4* src =
+            reinterpret_cast<const float4*>(p.u_rows + ((size_t)(mine ? tr : 0) * p.L + l) * p.R16 + 16 * q0);
+        float4 v[4 * kFpGroups];
+#pragma unroll
+        for (int g = 0; g < kFpGroups; ++g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v[4 * g + e] = mine && g < ng ? __ldcg(src + 4 * g + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         if (n >= kFpUBufs) {  // one lane waits for the buffer to be free; the warp follows it
           int got = 1;
           if (lane == 0) got = mbar_wait_or_fail(&uempty_bar[q], ((n / kFpUBufs) - 1) & 1, &fail_sh) ? 1 : 0;
@@ -349,25 +359,16 @@ __global__ void __launch_bounds__(kFpThreads, 1)
           }
         }
         uint8_t* ub = ubuf + (size_t)q * kFpUBufBytes;
-        const bool mine = myslot == k;
-        const float4* src =
-            reinterpret_cast<const float4*>(p.u_rows + ((size_t)(mine ? tr : 0) * p.L + l) * p.R16 + 16 * q0);
-        for (int g = 0; g < ng; ++g) {
-          float u[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 v = mine ? __ldcg(src + 4 * g + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            u[4 * e] = v.x;
-            u[4 * e + 1] = v.y;
-            u[4 * e + 2] = v.z;
-            u[4 * e + 3] = v.w;
-          }
+        for (int g = 0; g < kFpGroups; ++g) {
+          if (g >= ng) break;
 #pragma unroll
           for (int kc = 0; kc < 2; ++kc) {
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float u0 = u[8 * kc + 2 * e], u1 = u[8 * kc + 2 * e + 1];
+              const float4 f4 = v[4 * g + 2 * kc + (e >> 1)];
+              const float u0 = (e & 1) ? f4.z : f4.x, u1 = (e & 1) ? f4.w : f4.y;
               const __nv_bfloat16 h0 = __float2bfloat16_rn(u0), h1 = __float2bfloat16_rn(u1);
               const __nv_bfloat16 l0 = __float2bfloat16_rn(u0 - __bfloat162float(h0));
               const __nv_bfloat16 l1 = __float2bfloat16_rn(u1 - __bfloat162float(h1));

@@ -15,8 +15,8 @@
 //   1. K loop over d_in: TMA brings a 128 x 64 tile of x and a 256 x 64 tile of
 //      W (128-byte swizzle) per stage; one thread issues
 //      tcgen05.mma.kind::f16 (M = 128, N = 256, K = 16) into a 256-column fp32
-//      accumulator in tensor memory.  On prompt-like batches the CTAs work in
-//      pairs (a cluster of two) on 256 x 256 tiles with tcgen05's pair MMA
+//      accumulator in tensor memory.  On batches of long prompts the CTAs work
+//      in pairs (a cluster of two) on 256 x 256 tiles with tcgen05's pair MMA
 //      (cta_group::2, M = 256): each CTA loads its own 128 rows of x and 128
 //      of the tile's 256 W rows, so each SM moves a third fewer bytes through
 //      shared memory per flop and six 32 KB stages replace four of 48 KB.
@@ -60,10 +60,12 @@ constexpr int kFpBandTiles = 16;                              // row tiles per b
 constexpr int kFpSlotWords = LORA_MAX_SLOTS / 32;
 constexpr int kFpMaxStages = 6;
 constexpr int kFpMaxUBufs = 2;
-// Prompt-like batches (at least this many rows per sequence on average) run
-// in CTA pairs; decode batches, whose tiles hold many slots, in single CTAs,
-// whose expand steps are cheaper.  Both forms give every row the same bits.
-constexpr int kFpPairMinRowsPerSeq = 16;
+// Batches of long prompts (at least this many rows per sequence on average)
+// run in CTA pairs; the others, whose tiles hold more slots, in single CTAs,
+// whose expand steps are cheaper (a pair's steps follow the slots of both of
+// its tiles and wait on both CTAs' operand builders).  Both forms give every
+// row the same bits.
+constexpr int kFpPairMinRowsPerSeq = 256;
 
 // The two forms of the kernel: one CTA per 128 x 256 tile (kCta = 1), or a
 // CTA pair per 256 x 256 tile with tcgen05's pair MMA (kCta = 2): each CTA
@@ -606,8 +608,8 @@ int launch_fused_projection(const PoolView& pool, const lora_segments* seg, cons
   const int T = seg->T;
   if (T <= 0) return LORA_OK;
   const int ntm = ceil_div(T, kFpM);
-  // A CTA pair per 256 rows for prompt-like batches with two row tiles to
-  // pair (one row tile would leave every second CTA without rows).
+  // A CTA pair per 256 rows for batches of long prompts with two row tiles
+  // to pair (one row tile would leave every second CTA without rows).
   const int cta = ntm >= 2 && (long long)T >= (long long)kFpPairMinRowsPerSeq * seg->S ? 2 : 1;
   CUtensorMap tm_x, tm_w;
   {

@@ -283,8 +283,10 @@ int lora_apply_shrink_expand_noalloc(const lora_pool* pool, const lora_segments*
  *      stacked in lane order, as a linear layer stores [out][in]);
  *      ldw >= d_in, ldw % 8 == 0, 16-byte aligned.
  *   x, y, ldx, ldy: as for lora_apply_shrink_expand (y is written, not updated).
- * Arithmetic: one tcgen05 GEMM over tiles of 128 rows x 256 columns, bf16
- * products summed in fp32 over d_in in a fixed order; the expand of every slot
+ * Arithmetic: one tcgen05 GEMM over tiles of 128 rows x 256 columns (on
+ * batches of long prompts, 256 x 256 tiles on CTA pairs with the pair MMA;
+ * both forms give a row the same bits), bf16 products summed in fp32 over
+ * d_in in a fixed order; the expand of every slot
  * present in a tile goes into the same fp32 accumulator as MMAs whose
  * rank-space input is u' = scale * (A @ x) split into bf16 hi and lo halves
  * (u' from the two shrinks, run before it in a row mode that writes u' to the

@@ -201,15 +201,18 @@ __global__ void __launch_bounds__(kFpThreads, 1)
     }
     fail_sh = 0;
     stop_sh[0] = stop_sh[1] = 0;
-    if (kPair) {
+    fence_mbar_init();
+  }
+  if (kPair) {
+    // Both CTAs run and their barriers exist before either touches the
+    // other's shared memory; then each sends its reading of the status word.
+    cluster_sync_all();
+    if (threadIdx.x == 0) {
       const int bad = *p.status != 0 ? 1 : 0;
       bad_sh[rank] = bad;
       st_dsmem_u32(mapa_shared(smem_u32(&bad_sh[rank]), (uint32_t)(rank ^ 1)), (uint32_t)bad);
     }
-    fence_mbar_init();
-  }
-  if (kPair) {
-    cluster_sync_all();  // the peer's barriers exist, and both readings of the status are in
+    cluster_sync_all();
     if (bad_sh[0] | bad_sh[1]) return;
   }
   if (warp == 0) {

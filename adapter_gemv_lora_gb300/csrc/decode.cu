@@ -8,14 +8,18 @@
 //           scale * B @ (A @ x); xLLM PR #2014, shrink then expand)
 //
 // One kernel does both halves.  A work unit is (decode group, lane) and runs
-// on one thread-block cluster of CL CTAs (CL from the pool's shape only):
+// on one thread-block cluster of CL CTAs (CL from d_in only: 8 from d_in 8192
+// on, else 4 for d_in >= 256):
 //   1. CTA c of the cluster shrinks its fixed range of d_in (K blocks of 64,
 //      [c * nkb / CL, (c + 1) * nkb / CL)) for the group's rows: a partial
 //      rank-space vector of up to 8 rows x r16 ranks.
-//   2. Every CTA pushes its partial into every CTA's shared memory with
-//      st.async, counted on the receiver's mbarrier (no fence, no global
-//      memory); each CTA then adds the CL partials in CTA order.  So u never
-//      leaves the chip, and every CTA of the cluster holds the same u.
+//   2. The partials are reduced on chip in two rounds of st.async stores,
+//      each counted on the receiver's mbarrier (no fence, no global memory):
+//      every CTA sends each 1 / CL slice of its ranks to the CTA that owns
+//      the slice, which adds the CL partials in CTA order; then every owner
+//      sends its summed slice to every CTA.  So u never leaves the chip, every
+//      CTA of the cluster holds the same u, and the buffers hold R16 x 8
+//      floats a round whatever CL is.
 //   3. CTA c expands its own slice of the lane's output columns
 //      ([c * ncb / CL, (c + 1) * ncb / CL) in blocks of 64) and updates y.
 // The clusters are persistent (as many as fit on the GPU at once) and take
@@ -67,7 +71,6 @@ constexpr int kDfCols = 512;                      // expand columns per chunk, 4
 constexpr int kDfColsPerThread = kDfCols / kDfCompute;
 constexpr int kDfRanksPerPage = 16;               // B^T rank rows per page (16 x 512 bf16 = 16 KB)
 constexpr int kDfYPitch = kDfCols * 4;            // bytes per y row of a page
-constexpr int kDfUFloats = 128 * kDecGroup;       // u of a unit: [rank][row], ranks up to 128
 constexpr int kDfClassCache = 2048;               // units whose rank class is kept in shared memory
 static_assert(kDfColsPerThread == 4, "expand thread tile: 4 columns x 8 rows");
 static_assert(kDecGroup * kDfYPitch <= kDfPageBytes, "a y page holds the group's rows of one chunk");
@@ -317,18 +320,22 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
     dec_fused_kernel(const __grid_constant__ TmapSized tm_a, const __grid_constant__ TmapLanes tm_bt, DfParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kDfMaxPages], empty_bar[kDfMaxPages], precv[2];
-  __shared__ __align__(16) float us[kDfUFloats];  // the summed u of the current unit, [rank][row]
+  __shared__ __align__(8) uint64_t full_bar[kDfMaxPages], empty_bar[kDfMaxPages];
+  __shared__ __align__(8) uint64_t prs[2], pag[2];  // per unit parity: reduce-scatter and all-gather bytes
   __shared__ int fail_sh;
   __shared__ int stop_sh[2];
-  __shared__ int xok_sh[2];  // per unit parity: every partial of the cluster arrived
+  __shared__ int xok_sh[2];  // per unit parity: every partial of this CTA's rank slice arrived
+  __shared__ int xag_sh[2];  // per unit parity: every slice of u arrived
   __shared__ int8_t cls_sh[kDfClassCache];  // rank class of each unit (-1: nothing to do)
 
   uint8_t* smem = align1024(smem_raw);
   const uint32_t npages = (uint32_t)p.npages;
   uint8_t* ring = smem;  // npages pages, 1024-aligned
-  // partials received from the cluster's CTAs: [parity][ncta][R16 * 8] floats
-  float* recv = reinterpret_cast<float*>(smem + (size_t)npages * kDfPageBytes);
+  // exchange buffers after the ring, per unit parity: the partials of this
+  // CTA's rank slice from every CTA ([source CTA][slice rank][row]), then the
+  // whole summed u ([rank][row]); R16 x 8 floats each whatever the cluster size
+  float* rsbuf = reinterpret_cast<float*>(smem + (size_t)npages * kDfPageBytes);
+  float* agbuf = rsbuf + 2 * (size_t)p.R16 * kDecGroup;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = (int)cluster_ctarank(), ncta = (int)cluster_nctarank();
@@ -341,8 +348,10 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
     }
     // per unit parity: one local arrival (with the expected bytes) and the
     // st.async bytes of every CTA's partial
-    mbar_init(&precv[0], 1);
-    mbar_init(&precv[1], 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&prs[q], 1);
+      mbar_init(&pag[q], 1);
+    }
     fail_sh = 0;
     fence_mbar_init();
   }
@@ -462,10 +471,14 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
       if (stop_sh[dj & 1]) break;
       ++dj;
       bool ok = true;
-      float* rbuf = recv + (size_t)(uj & 1) * ncta * part_floats;
-      uint64_t* pr = &precv[uj & 1];
+      const int par = (int)(uj & 1);
+      float* rs = rsbuf + (size_t)par * part_floats;
+      float* ag = agbuf + (size_t)par * part_floats;
       // this CTA expects every CTA's partial of this unit (st.async bytes)
-      if (t == 0) mbar_expect_tx(pr, (uint32_t)(ncta * U.r16 * kDecGroup * 4));
+      if (t == 0) {  // this CTA receives r16 x 8 floats in each of the two rounds
+        mbar_expect_tx(&prs[par], (uint32_t)(U.r16 * kDecGroup * 4));
+        mbar_expect_tx(&pag[par], (uint32_t)(U.r16 * kDecGroup * 4));
+      }
       // ---- shrink of this CTA's K range: thread tile rtile rows x 4 ranks
       const int rtile = U.nrows <= 1 ? 1 : U.nrows <= 2 ? 2 : U.nrows <= 4 ? 4 : 8;
       const int rt = t / U.nks, ks = t - rt * U.nks;
@@ -529,38 +542,49 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
           nout = 8;
         }
         if (active) {
-          // slot `cta` of every CTA's receive buffer, counted on its barrier
-          const uint32_t slot = smem_u32(rbuf + (size_t)cta * part_floats), bar = smem_u32(pr);
-          for (int c = 0; c < ncta; ++c) {
-            const uint32_t dst = mapa_shared(slot, (uint32_t)c), dbar = mapa_shared(bar, (uint32_t)c);
+          // reduce-scatter: rank i goes to the CTA owning its slice of r16 /
+          // CL ranks, into that CTA's row for this source CTA
+          const int slice = U.r16 / ncta;
+          const uint32_t rs_a = smem_u32(rs), bar = smem_u32(&prs[par]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              if (e < nout) {
-                const int o = out0 + e, g = o >> 2, i = 4 * rt + (o & 3);
-                st_async_f32(dst + 4u * (uint32_t)(i * kDecGroup + g), v[e], dbar);
-              }
+          for (int e = 0; e < 8; ++e) {
+            if (e < nout) {
+              const int o = out0 + e, g = o >> 2, i = 4 * rt + (o & 3);
+              const int dest = i / slice, li = i - dest * slice;
+              st_async_f32(mapa_shared(rs_a + 4u * (uint32_t)((cta * slice + li) * kDecGroup + g), (uint32_t)dest),
+                           v[e], mapa_shared(bar, (uint32_t)dest));
             }
           }
         }
       }
-      // ---- u = the sum of the CL partials in CTA order: one thread waits for
-      // the bytes, then releases the other compute threads
+      // ---- u of this CTA's rank slice = the sum of the CL partials in CTA
+      // order (one thread waits for the bytes, then releases the others);
+      // then all-gather: the slice to every CTA of the cluster
       if (t == 0) {
-        const bool got = mbar_wait_or_fail(pr, (uj >> 1) & 1, &fail_sh);
+        const bool got = mbar_wait_or_fail(&prs[par], (uj >> 1) & 1, &fail_sh);
         if (!got) fail_sh = 1;
-        xok_sh[uj & 1] = got ? 1 : 0;
+        xok_sh[par] = got ? 1 : 0;
       }
       named_bar_sync(1, kDfCompute);
-      if (!xok_sh[uj & 1]) ok = false;
+      if (!xok_sh[par]) ok = false;
       if (ok) {
-        for (int idx = t; idx < U.r16 * kDecGroup; idx += kDfCompute) {
-          float sum = rbuf[idx];
-          for (int c = 1; c < ncta; ++c) sum += rbuf[(size_t)c * part_floats + idx];
-          us[idx] = sum;
+        const int n_el = (U.r16 / ncta) * kDecGroup;
+        const uint32_t ag_a = smem_u32(ag) + 4u * (uint32_t)(cta * n_el), bar = smem_u32(&pag[par]);
+        for (int idx = t; idx < n_el; idx += kDfCompute) {
+          float sum = rs[idx];
+          for (int c = 1; c < ncta; ++c) sum += rs[(size_t)c * n_el + idx];
+          for (int c = 0; c < ncta; ++c)
+            st_async_f32(mapa_shared(ag_a + 4u * (uint32_t)idx, (uint32_t)c), sum, mapa_shared(bar, (uint32_t)c));
         }
+      }
+      if (t == 0) {
+        const bool got = ok && mbar_wait_or_fail(&pag[par], (uj >> 1) & 1, &fail_sh);
+        if (ok && !got) fail_sh = 1;
+        xag_sh[par] = got ? 1 : 0;
       }
       ++uj;
       named_bar_sync(1, kDfCompute);  // u complete
+      if (!xag_sh[par]) ok = false;
       if (p.u_rows) {  // row mode: scale * u of the group's rows, written once (by CTA 0)
         if (ok && cta == 0) {
           const float sc = p.scale_tab[U.k * p.L + U.l];
@@ -568,7 +592,7 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
           for (int g = 0; g < kDecGroup; ++g) {
             if (g < U.nrows) {
               float* dst = p.u_rows + ((size_t)U.row[g] * p.L + U.l) * p.R16;
-              for (int i = t; i < U.r16; i += kDfCompute) dst[i] = sc * us[i * kDecGroup + g];
+              for (int i = t; i < U.r16; i += kDfCompute) dst[i] = sc * ag[i * kDecGroup + g];
             }
           }
         }
@@ -594,10 +618,10 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
           if (ok && has) {
             const uint8_t* bp = ring + (size_t)s * kDfPageBytes + b_off;
             const int nr = min(kDfRanksPerPage, U.r - rb);
-            if (rtile == 1) expand_page<1>(bp, 2 * U.bi, us, rb, nr, eacc);
-            else if (rtile == 2) expand_page<2>(bp, 2 * U.bi, us, rb, nr, eacc);
-            else if (rtile == 4) expand_page<4>(bp, 2 * U.bi, us, rb, nr, eacc);
-            else expand_page<8>(bp, 2 * U.bi, us, rb, nr, eacc);
+            if (rtile == 1) expand_page<1>(bp, 2 * U.bi, ag, rb, nr, eacc);
+            else if (rtile == 2) expand_page<2>(bp, 2 * U.bi, ag, rb, nr, eacc);
+            else if (rtile == 4) expand_page<4>(bp, 2 * U.bi, ag, rb, nr, eacc);
+            else expand_page<8>(bp, 2 * U.bi, ag, rb, nr, eacc);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -645,7 +669,7 @@ int dec_group_bound(const PoolView& pool, const lora_segments* seg) {
 // its bits, depends neither on the batch nor on the pool's rank padding.
 int cluster_size(const PoolView& pool) {
   const int nkb = pool.d_in / 64;
-  return nkb >= 4 ? 4 : (nkb >= 2 ? 2 : 1);
+  return nkb >= 128 ? 8 : nkb >= 4 ? 4 : (nkb >= 2 ? 2 : 1);
 }
 
 // Ring pages: as many 18 KB pages as the shared memory left to each of the
@@ -665,13 +689,13 @@ int dec_pages(const PoolView& pool, int ncta) {
   // most 227 KiB per CTA
   long long per_cta = 233472 / kDfCtasPerSm - 1024;
   if (per_cta > 232448) per_cta = 232448;
-  const long long recv = 2LL * ncta * pool.R16 * kDecGroup * 4;
+  const long long recv = 4LL * pool.R16 * kDecGroup * 4;  // exchange buffers: two rounds x two parities
   const long long pages = (per_cta - st - 1024 - recv) / kDfPageBytes;
   return (int)(pages < kDfMaxPages ? pages : kDfMaxPages);
 }
 
 size_t dec_smem_bytes(const PoolView& pool, int ncta, int npages) {
-  return 1024 + (size_t)npages * kDfPageBytes + (size_t)2 * ncta * pool.R16 * kDecGroup * 4;
+  return 1024 + (size_t)npages * kDfPageBytes + (size_t)4 * pool.R16 * kDecGroup * 4;
 }
 
 // Clusters that can be resident at once, per (device, cluster size, shared memory).

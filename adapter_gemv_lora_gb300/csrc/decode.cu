@@ -189,10 +189,10 @@ __device__ __forceinline__ int unit_class(const DfParams& p, const int8_t* cls_s
 }
 
 __device__ __forceinline__ void unit_iter_init(UnitIter& it, const DfParams& p, const int8_t* cls_sh, int n_units,
-                                               int lane) {
+                                               int n_clusters, int lane) {
   it.n_units = n_units;
   it.q = (int)cluster_id_x();
-  it.nc = (int)num_clusters_x();
+  it.nc = n_clusters;
   unsigned present = 0;
   for (int u0 = 0; u0 < n_units; u0 += 32) {
     const int c = u0 + lane < n_units ? unit_class(p, cls_sh, u0 + lane) : -1;
@@ -346,8 +346,8 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kDfComputeWarps);
     }
-    // per unit parity: one local arrival (with the expected bytes) and the
-    // st.async bytes of every CTA's partial
+    // per unit parity, for each exchange round: one local arrival (with the
+    // expected bytes) and the st.async bytes the other CTAs send
     for (int q = 0; q < 2; ++q) {
       mbar_init(&prs[q], 1);
       mbar_init(&pag[q], 1);
@@ -366,17 +366,28 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
   // two), each its own unit that redoes the pair's shrink, so more clusters
   // work.  Every CTA computes the same value from the same counts, and a
   // row's bits do not depend on it.
+  // Clusters at work: all, unless the step's tensor tiles (whose kernels run
+  // beside this one on another stream) outweigh its decode units (a tile of up
+  // to 128 rows against a group of up to 8: four units to a tile); then the
+  // tensor path bounds the step, and only as many clusters work as give each
+  // about four units (no column parts), which leaves the SMs to the tensor
+  // path while the decode units still finish within its time.  Idle clusters
+  // leave at once.
+  const int pairs = p.counts[2] * p.L;
+  const bool beside_tensor = p.counts[3] > 0 && 4LL * p.counts[3] >= pairs;
+  int n_clusters = (int)num_clusters_x();
+  if (beside_tensor) n_clusters = min(n_clusters, max(1, (pairs + 3) / 4));
+  if ((int)cluster_id_x() >= n_clusters) return;  // every CTA of the cluster alike
   {
-    const int pairs = p.counts[2] * p.L;
     int parts = 1;
-    while (!p.u_rows && parts < 4 && pairs * parts * 2 <= (int)num_clusters_x()) parts *= 2;
+    while (!p.u_rows && !beside_tensor && parts < 4 && pairs * parts * 2 <= n_clusters) parts *= 2;
     p.parts = parts;
   }
   const int n_units = p.counts[2] * p.L * p.parts;
   for (int u = tid; u < n_units && u < kDfClassCache; u += kDfThreads) cls_sh[u] = (int8_t)unit_class_global(p, u);
   __syncthreads();
   UnitIter it;
-  unit_iter_init(it, p, cls_sh, n_units, lane);
+  unit_iter_init(it, p, cls_sh, n_units, n_clusters, lane);
 
   if (warp == kDfComputeWarps) {
     // ---------------- producer: per A page the group's x rows and the slot's

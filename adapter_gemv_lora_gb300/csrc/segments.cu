@@ -178,7 +178,7 @@ template <bool SEQ_SMEM>
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) {
   extern __shared__ int smem_dyn[];
   __shared__ int scan_sums[3][33];
-  __shared__ int bad_sh;
+  __shared__ int bad_sh, long_sh;
   __shared__ unsigned long long len_sh;
   pdl_launch_next();  // the apply kernels may be scheduled now; they wait for this grid
   pdl_wait();         // the previous kernel's results are visible from here on
@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   for (int i = tid; i < N; i += kSegThreads) cnt_tile[i] = 0;
   if (tid == 0) {
     bad_sh = 0;
+    long_sh = 0;
     len_sh = 0ull;
   }
 
@@ -263,9 +264,11 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
       const int wb = (int)__reduce_or_sync(0xffffffffu, (unsigned)bad);
+      const bool wlong = __any_sync(0xffffffffu, len > kShortSeq);
       if (lane == 0) {
         if (wb) atomicOr(&bad_sh, wb);
         if (wl) atomicAdd(&len_sh, (unsigned long long)wl);
+        if (wlong) long_sh = 1;
       }
     }
     if (s < S) {
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
         p.tc_work[base + i] = make_int4(id, rb, min(rb + kTcTile, st + len), s);
     }
   }
-  {
+  if (long_sh) {  // a step of decode rows only has none
     int n_long = 0;  // long sequences before this chunk
     for (int b = 0; b < S; b += 32) {
       const int s = b + lane;

@@ -48,8 +48,9 @@ struct SegParams {
 };
 
 // Exclusive prefix sum over the block (all threads call it).  `sums` is a
-// shared array of >= 33 ints.  Returns the prefix and sets `total`.
-__device__ int block_exclusive_scan(int v, int* sums, int& total) {
+// shared array of >= 33 ints.  Returns the prefix and sets `total`.  Without
+// `reuse_sync` the caller must pass a barrier before `sums` is written again.
+__device__ int block_exclusive_scan(int v, int* sums, int& total, bool reuse_sync) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -73,7 +74,7 @@ __device__ int block_exclusive_scan(int v, int* sums, int& total) {
   __syncthreads();
   const int ex = sums[warp] + x - v;
   total = sums[32];
-  __syncthreads();
+  if (reuse_sync) __syncthreads();
   return ex;
 }
 
@@ -180,9 +181,6 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
   __shared__ int scan_sums[3][33];
   __shared__ int bad_sh, long_sh;
   __shared__ unsigned long long len_sh;
-  pdl_launch_next();  // the apply kernels may be scheduled now; they wait for this grid
-  pdl_wait();         // the previous kernel's results are visible from here on
-
   const int N = p.N, Scap = p.S, T = p.T;
   int* cnt_tok = smem_dyn;         // [2N] rows per (class, slot), then their first perm position
   int* run_tok = cnt_tok + 2 * N;  // [2N] running position while ranking sequences
@@ -202,16 +200,23 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kLeadShift = 24, kKeyMask = (1 << kLeadShift) - 1;  // keys < 2N <= 4096
-  // the sequence count (from the device when a run-length pass wrote it)
-  const int S = p.S_dev ? min(max(*p.S_dev, 0), Scap) : Scap;
 
+  // Shared state first: it does not depend on the previous kernel, so it is
+  // set while that kernel finishes.  The rank tables start at zero; each
+  // chunk's last pass over them sets them back to zero.
   for (int i = tid; i < 2 * N; i += kSegThreads) run_tok[i] = 0;
   for (int i = tid; i < N; i += kSegThreads) cnt_tile[i] = 0;
+  if (p.tables)
+    for (int i = tid; i < kSegWarps * 3 * N; i += kSegThreads) tab_rows[i] = 0;
   if (tid == 0) {
     bad_sh = 0;
     long_sh = 0;
     len_sh = 0ull;
   }
+  pdl_launch_next();  // the apply kernels may be scheduled now; they wait for this grid
+  pdl_wait();         // the previous kernel's results are visible from here on
+  // the sequence count (from the device when a run-length pass wrote it)
+  const int S = p.S_dev ? min(max(*p.S_dev, 0), Scap) : Scap;
 
   // ---- per sequence, 512 at a time: length, slot, key, first row (block
   // scan), and its rank among the earlier lanes of its warp with the same
@@ -256,7 +261,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
       }
     }
     int tot;
-    const int ex = block_exclusive_scan(s < S ? len : 0, scan_sums[0], tot);
+    // (with the tables, their two barriers below come before the sums are reused)
+    const int ex = block_exclusive_scan(s < S ? len : 0, scan_sums[0], tot, !p.tables);
     {
       // validation: order-free reductions, one shared atomic per warp and chunk
       // (after the scan's barriers, so after thread 0 cleared the sums)
@@ -285,8 +291,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
       // running counts of the earlier chunks; then the counts advance
       const bool tc = key >= N;
       const int id = tc ? key - N : key;
-      for (int i = tid; i < kSegWarps * 3 * N; i += kSegThreads) tab_rows[i] = 0;
-      __syncthreads();
+      // (the tables are zero: cleared before the first chunk, and by the
+      // previous chunk's last pass, both ordered by the scan's barriers)
       if (key >= 0 && lead == lane) {
         tab_rows[warp * 2 * N + key] = pl + len;
         if (tc) tab_tiles[warp * N + id] = pt + nt;
@@ -301,17 +307,23 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p) 
         s_pos[s] = br + pl;
         if (tc) s_tile[s] = bt + pt;
       }
-      __syncthreads();  // every read of the running counts is done
+      __syncthreads();  // every read of the running counts and of the tables is done
       for (int k = tid; k < 2 * N; k += kSegThreads) {
         int add = 0;
 #pragma unroll
-        for (int w = 0; w < kSegWarps; ++w) add += tab_rows[w * 2 * N + k];
+        for (int w = 0; w < kSegWarps; ++w) {
+          add += tab_rows[w * 2 * N + k];
+          tab_rows[w * 2 * N + k] = 0;
+        }
         run_tok[k] += add;
       }
       for (int k = tid; k < N; k += kSegThreads) {
         int add = 0;
 #pragma unroll
-        for (int w = 0; w < kSegWarps; ++w) add += tab_tiles[w * N + k];
+        for (int w = 0; w < kSegWarps; ++w) {
+          add += tab_tiles[w * N + k];
+          tab_tiles[w * N + k] = 0;
+        }
         cnt_tile[k] += add;
       }
       // the next chunk's block scan has barriers before its tables are cleared
@@ -482,7 +494,7 @@ __global__ void __launch_bounds__(kRunThreads, 1) moe_runs_kernel(MoeRunParams p
       slot = (e < 0 || e >= p.E || a < 0 || a > p.A) ? p.N : (a == 0 ? 0 : 1 + e * p.A + (a - 1));
     }
     int tot;
-    const int idx = carry + block_exclusive_scan(flag, sums, tot);
+    const int idx = carry + block_exclusive_scan(flag, sums, tot, true);
     if (flag && idx < p.cap) {
       p.run_ids[idx] = slot;
       p.run_starts[idx] = r;

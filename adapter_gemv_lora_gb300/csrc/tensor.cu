@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 }
 
 // Expand CTA: warp 0 TMA, warp 1 MMA, warps 2-5 read TMEM (one lane quadrant
-// each) and stage scale * acc in shared memory, warps 6-13 do the y update with
+// each) and stage scale * acc in shared memory, warps 6-21 do the y update with
 // coalesced 128-bit loads and stores (two 256-byte row segments per warp
 // instruction, the next half-chunk's y loads in flight while the current one
 // is added).  Rows past the end of the tile's sequence are skipped.
@@ -374,7 +374,7 @@ constexpr int kExpRmwWarps = 16;
 constexpr int kExpThreads = (2 + kExpTmemWarps + kExpRmwWarps) * 32;
 constexpr int kHalfCols = 64;                          // columns per staged half chunk
 constexpr int kHalfBytes = kTcTile * kHalfCols * 4;    // 32 KB
-constexpr int kRmwRowsPerWarp = kTcTile / kExpRmwWarps;  // 16
+constexpr int kRmwRowsPerWarp = kTcTile / kExpRmwWarps;  // 8
 
 __global__ void __launch_bounds__(kExpThreads, 1)
     tc_expand_kernel(const __grid_constant__ TmapSized tm_b, TcExpandParams p) {

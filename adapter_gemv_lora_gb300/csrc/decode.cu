@@ -90,6 +90,7 @@ struct DfParams {
   int64_t ldy;
   float* u_rows;  // row mode: scale * u of each row to [T][L][R16], no expand (y is not touched)
   int L, R16, nkb, npages;
+  int n_tab;  // entries of the rank and scale tables (slots x lanes)
   int parts;  // column parts per (group, lane), each its own unit (set on the device per step)
   int d_out[LORA_MAX_LANES], off[LORA_MAX_LANES], bt_cols[LORA_MAX_LANES];
 };
@@ -340,7 +341,9 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = (int)cluster_ctarank(), ncta = (int)cluster_nctarank();
   const int part_floats = p.R16 * kDecGroup;
-  pdl_wait();  // the segment builder's results are visible from here on
+  // Barriers, the cluster's meeting and the pool's tables and TMA descriptors
+  // do not depend on the previous kernel: they are set up and warmed while it
+  // finishes (the tables were written when the adapters were loaded).
   if (tid == 0) {
     for (uint32_t s = 0; s < npages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -355,8 +358,23 @@ __global__ void __launch_bounds__(kDfThreads, kDfCtasPerSm)
     fail_sh = 0;
     fence_mbar_init();
   }
+  if (tid == kDfCompute) {  // the producer's lane 0, with constant indexes into the parameters
+#pragma unroll
+    for (int l = 0; l < LORA_MAX_LANES; ++l) {
+      if (l < p.L) {
+#pragma unroll
+        for (int sz = 0; sz < kTmapSizes; ++sz) prefetch_tensormap(&tm_a.m[sz][l]);
+        prefetch_tensormap(&tm_bt.m[l]);
+      }
+    }
+  }
+  for (int i = tid * 32; i < p.n_tab; i += kDfThreads * 32) {
+    prefetch_l2(p.rank_tab + i);
+    prefetch_l2(p.scale_tab + i);
+  }
   // every CTA's barriers are initialised before any CTA stores into it
   cluster_sync_all();
+  pdl_wait();  // the segment builder's results are visible from here on
 
   // Units (decode group, lane), longest first (UnitIter).  The counts are
   // final before this grid runs (the builder wrote them; a builder error
@@ -795,6 +813,7 @@ int decode_impl(const PoolView& pool, const lora_segments* seg, const uint16_t* 
   p.R16 = pool.R16;
   p.nkb = pool.d_in / 64;
   p.npages = npages;
+  p.n_tab = pool.N * pool.L;
   p.parts = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * ncta));
